@@ -1,0 +1,24 @@
+"""fp64 CPU oracle of the Skip Softmax attention path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+package: only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline``
+and reference legs of ``bench.py`` use it.  It shares no code with the CUDA
+library; the only common dependency is the seeded input generator ``synth``.
+
+Parity is pinned for every function here (see ``tests/test_oracle_pins.py``):
+dense attention from a library routine at lambda = 0, an independent
+closed-form skip mask, a closed-form output over the kept keys, monotonicity
+in lambda, the analytic error bound, and hand-derived worked examples.
+"""
+
+from .skipsm_oracle import (  # noqa: F401
+    PrefillResult,
+    DecodeResult,
+    prefill,
+    prefill_qtile,
+    decode,
+    decode_group,
+    decode_split_geometry,
+    dense_attention,
+    skipped_mass,
+)

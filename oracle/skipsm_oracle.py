@@ -1,0 +1,307 @@
+"""Plain fp64 implementation of Skip Softmax attention (prefill and decode).
+
+TEST INFRASTRUCTURE ONLY: the CUDA library never imports this module.
+
+What it computes, and where the pages say so
+--------------------------------------------
+* "Accelerating Long-Context Inference with Skip Softmax in NVIDIA TensorRT-LLM"
+  (video recap), sections "Quick Overview", "Detailed Analysis" and "Skip
+  Softmax Mechanism": attention is processed block by block; the local maximum
+  of a block's attention scores is compared with the maximum seen before it
+  (printed "MI - 1", read here as m_{i-1}, the running maximum over the blocks
+  already processed), and when the block falls below the threshold tau its whole
+  attention computation is skipped.  "Impact on Accuracy vs. Speed": tau trades
+  speed for accuracy.
+* "NVIDIA Introduces Skip Softmax for Enhanced LLM Inference Efficiency",
+  section "Understanding Skip Softmax": blocks whose contribution is negligible
+  are detected early from the softmax's own properties and skipped, with no
+  retraining.
+* The exact rule used here (the plainest reading the pages support): for a
+  (query tile, key tile) pair, with m~_r the tile's row maximum of the scaled
+  logits and m_r the running row maximum before the tile, the tile is skipped
+  iff lambda > 0 and, for every valid row r of the query tile,
+  exp(m~_r - m_r) < lambda, i.e. m~_r - m_r < ln(lambda).  A skipped tile
+  contributes nothing (no exponentials, no P.V); a kept tile takes the exact
+  online-softmax update (the FlashAttention recurrence named in "Approximating
+  Softmax in Pretrained LLMs", Abstract).
+
+Readings where the pages are silent
+-----------------------------------
+* key tiles are visited in ascending order; the running max starts at -inf, so
+  the first visited tile is never skipped (gap = +inf);
+* a row with no visible key in the tile has gap -inf (it votes "skip");
+* padding rows beyond Sq do not vote;
+* causal masking is bottom-right aligned: query i sits at position Skv-Sq+i;
+* softmax scale 1/sqrt(D) unless given;
+* decode: the rows of one vote are the G query heads that share a kv head; the
+  cache is cut into contiguous splits of whole key tiles (ceil(nblk/splits)
+  tiles each, empty trailing splits dropped); every split starts its own
+  running max at -inf and the split results are merged by an exact
+  log-sum-exp combine.
+
+Everything is fp64; bf16 inputs convert to fp64 exactly.  There is no blocking,
+fusion or reordering beyond the tile loop that defines the method.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import List, Optional, Tuple
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+# ---------------------------------------------------------------------------
+# the steps of one (query tile, key tile) visit
+# ---------------------------------------------------------------------------
+def _tile_logits(qrows: np.ndarray, ktile: np.ndarray, scale: float, qpos: np.ndarray,
+                 kidx: np.ndarray, causal: bool) -> np.ndarray:
+    """Scaled logits s_rc = (q_r . k_c) * scale, -inf where key c is not visible."""
+    s = (qrows @ ktile.T) * scale
+    if causal:
+        s = np.where(kidx[None, :] > qpos[:, None], NEG_INF, s)
+    return s
+
+
+def _row_gap(m_loc: np.ndarray, m_run: np.ndarray) -> np.ndarray:
+    """Gap d_r = m~_r - m_r, with -inf for an empty row and +inf before any key."""
+    with np.errstate(invalid="ignore"):
+        d = m_loc - m_run
+    d = np.where(m_run == NEG_INF, np.inf, d)
+    d = np.where(m_loc == NEG_INF, NEG_INF, d)
+    return d
+
+
+def _vote(d: np.ndarray, lam: float) -> Tuple[bool, float]:
+    """Skip iff lambda > 0 and every row has d_r < ln(lambda).
+
+    Returns (skip, margin) where margin = |max_r d_r - ln(lambda)| in nats is
+    how far the decision is from flipping (+inf when it cannot flip).
+    """
+    if lam <= 0.0:
+        return False, math.inf
+    thr = math.log(lam)
+    dmax = float(np.max(d))
+    skip = bool(np.all(d < thr))
+    margin = math.inf if math.isinf(dmax) else abs(dmax - thr)
+    return skip, margin
+
+
+def _online_update(m: np.ndarray, l: np.ndarray, o: np.ndarray, s: np.ndarray,
+                   vtile: np.ndarray):
+    """Exact online-softmax update of (running max, row sum, output) by one tile."""
+    m_new = np.maximum(m, np.max(s, axis=1))
+    with np.errstate(invalid="ignore"):
+        alpha = np.where(m == NEG_INF, 0.0, np.exp(m - m_new))
+        p = np.where(s == NEG_INF, 0.0, np.exp(s - m_new[:, None]))
+    l_new = alpha * l + p.sum(axis=1)
+    o_new = alpha[:, None] * o + p @ vtile
+    return m_new, l_new, o_new
+
+
+def _finish(m: np.ndarray, l: np.ndarray, o: np.ndarray):
+    return o / l[:, None], m + np.log(l)
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+@dataclass
+class PrefillResult:
+    o: np.ndarray       # [B][Hq][Sq][D]
+    lse: np.ndarray     # [B][Hq][Sq] natural log
+    mask: np.ndarray    # int8 [B][Hq][nqt][nkt]: -1 not visited, 0 kept, 1 skipped
+    margin: np.ndarray  # fp64, same shape; +inf where the decision cannot flip
+
+    @property
+    def skip_counts(self) -> np.ndarray:
+        """Skipped tiles per query head, summed over batch and query tiles."""
+        return (self.mask == 1).sum(axis=(0, 2, 3))
+
+    @property
+    def visited_counts(self) -> np.ndarray:
+        return (self.mask >= 0).sum(axis=(0, 2, 3))
+
+
+def last_visible_key(r1: int, Sq: int, Skv: int, causal: bool) -> int:
+    """Last key index any row < r1 of the query tile can see."""
+    return min(Skv - 1, r1 - 1 + (Skv - Sq)) if causal else Skv - 1
+
+
+def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, tile_q: int,
+                  tile_k: int, causal: bool, lam: float, scale: float):
+    """One query tile of one head: returns (o_rows, lse_rows, mask[nkt], margin[nkt]).
+
+    qh is the head's full query matrix [Sq][D]; kh, vh its kv head [Skv][D].
+    """
+    Sq, Skv = qh.shape[0], kh.shape[0]
+    nkt = (Skv + tile_k - 1) // tile_k
+    r0, r1 = t * tile_q, min((t + 1) * tile_q, Sq)
+    qrows = qh[r0:r1]
+    qpos = np.arange(r0, r1) + (Skv - Sq)
+    n = r1 - r0
+    m = np.full(n, NEG_INF)
+    l = np.zeros(n)
+    o = np.zeros((n, qh.shape[1]))
+    mask = np.full(nkt, -1, dtype=np.int8)
+    margin = np.full(nkt, np.inf)
+    last_tile = last_visible_key(r1, Sq, Skv, causal) // tile_k
+    for j in range(last_tile + 1):
+        c0, c1 = j * tile_k, min((j + 1) * tile_k, Skv)
+        s = _tile_logits(qrows, kh[c0:c1], scale, qpos, np.arange(c0, c1), causal)
+        d = _row_gap(np.max(s, axis=1), m)
+        skip, mg = _vote(d, lam)
+        mask[j] = 1 if skip else 0
+        margin[j] = mg
+        if skip:
+            continue
+        m, l, o = _online_update(m, l, o, s, vh[c0:c1])
+    o, lse = _finish(m, l, o)
+    return o, lse, mask, margin
+
+
+def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: float,
+            tile_q: int, tile_k: int, scale: Optional[float] = None) -> PrefillResult:
+    """Skip Softmax prefill over q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] (fp64)."""
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if Hq % Hkv or (causal and Sq > Skv):
+        raise ValueError("invalid shapes")
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    nqt = (Sq + tile_q - 1) // tile_q
+    nkt = (Skv + tile_k - 1) // tile_k
+    o = np.zeros((B, Hq, Sq, D))
+    lse = np.zeros((B, Hq, Sq))
+    mask = np.full((B, Hq, nqt, nkt), -1, dtype=np.int8)
+    margin = np.full((B, Hq, nqt, nkt), np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // G], v[b, h // G]
+            for t in range(nqt):
+                r0, r1 = t * tile_q, min((t + 1) * tile_q, Sq)
+                ot, lt, mt, gt = prefill_qtile(q[b, h], kh, vh, t, tile_q=tile_q, tile_k=tile_k,
+                                               causal=causal, lam=lam, scale=scale)
+                o[b, h, r0:r1], lse[b, h, r0:r1] = ot, lt
+                mask[b, h, t], margin[b, h, t] = mt, gt
+    return PrefillResult(o, lse, mask, margin)
+
+
+# ---------------------------------------------------------------------------
+# decode (split-KV, one query token per sequence)
+# ---------------------------------------------------------------------------
+@dataclass
+class DecodeResult:
+    o: np.ndarray       # [B][Hq][D]
+    lse: np.ndarray     # [B][Hq]
+    mask: np.ndarray    # int8 [B][Hkv][nblk]: 0 kept, 1 skipped
+    margin: np.ndarray  # [B][Hkv][nblk]
+    num_splits: int     # splits actually used (after dropping empty ones)
+
+    @property
+    def skip_counts(self) -> np.ndarray:
+        """Skipped key tiles per query head: a group's count is given to each of its heads."""
+        B, Hkv, _ = self.mask.shape
+        G = self.o.shape[1] // Hkv
+        return np.repeat((self.mask == 1).sum(axis=(0, 2)), G)
+
+
+def decode_split_geometry(Skv: int, tile_k: int, num_splits: int) -> Tuple[int, int, int]:
+    """(key tiles, tiles per split, non-empty splits) of a split-KV decode."""
+    nblk = (Skv + tile_k - 1) // tile_k
+    per = (nblk + num_splits - 1) // num_splits
+    return nblk, per, (nblk + per - 1) // per
+
+
+def decode_group(qg: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, lam: float,
+                 num_splits: int, tile_k: int = 64, scale: Optional[float] = None):
+    """One GQA group: qg [G][D] against kv head kh, vh [Skv][D].
+
+    Returns (o [G][D], lse [G], mask [nblk], margin [nblk], per-split (o, lse) list).
+    """
+    G, D = qg.shape
+    Skv = kh.shape[0]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    nblk, per, nsplit = decode_split_geometry(Skv, tile_k, num_splits)
+    mask = np.zeros(nblk, dtype=np.int8)
+    margin = np.full(nblk, np.inf)
+    parts: List[Tuple[np.ndarray, np.ndarray]] = []
+    for sp in range(nsplit):
+        m = np.full(G, NEG_INF)
+        l = np.zeros(G)
+        o = np.zeros((G, D))
+        for j in range(sp * per, min((sp + 1) * per, nblk)):
+            c0, c1 = j * tile_k, min((j + 1) * tile_k, Skv)
+            s = _tile_logits(qg, kh[c0:c1], scale, np.zeros(G), np.arange(c0, c1), False)
+            d = _row_gap(np.max(s, axis=1), m)
+            skip, mg = _vote(d, lam)
+            mask[j] = 1 if skip else 0
+            margin[j] = mg
+            if skip:
+                continue
+            m, l, o = _online_update(m, l, o, s, vh[c0:c1])
+        parts.append(_finish(m, l, o))
+    # exact log-sum-exp combine of the split results
+    lses = np.stack([p[1] for p in parts])          # [nsplit][G]
+    top = lses.max(axis=0)
+    wts = np.exp(lses - top[None, :])
+    o = sum(wts[i][:, None] * parts[i][0] for i in range(nsplit)) / wts.sum(axis=0)[:, None]
+    lse = top + np.log(wts.sum(axis=0))
+    return o, lse, mask, margin, parts
+
+
+def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, lam: float, num_splits: int,
+           tile_k: int = 64, scale: Optional[float] = None) -> DecodeResult:
+    """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] (fp64)."""
+    B, Hq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    nblk, _, nsplit = decode_split_geometry(Skv, tile_k, num_splits)
+    o = np.zeros((B, Hq, D))
+    lse = np.zeros((B, Hq))
+    mask = np.zeros((B, Hkv, nblk), dtype=np.int8)
+    margin = np.zeros((B, Hkv, nblk))
+    for b in range(B):
+        for hk in range(Hkv):
+            og, lg, mg, gg, _ = decode_group(q[b, hk * G:(hk + 1) * G], k[b, hk], v[b, hk],
+                                             lam=lam, num_splits=num_splits, tile_k=tile_k,
+                                             scale=scale)
+            o[b, hk * G:(hk + 1) * G], lse[b, hk * G:(hk + 1) * G] = og, lg
+            mask[b, hk], margin[b, hk] = mg, gg
+    return DecodeResult(o, lse, mask, margin, nsplit)
+
+
+# ---------------------------------------------------------------------------
+# dense attention and the skipped probability mass (diagnostics)
+# ---------------------------------------------------------------------------
+def dense_attention(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, causal: bool,
+                    scale: Optional[float] = None, key_keep: Optional[np.ndarray] = None):
+    """Plain softmax(q k^T * scale + mask) v for one head; returns (o, lse, p).
+
+    key_keep, if given, is a boolean [Sq][Skv] matrix of keys allowed per row.
+    """
+    Sq, D = qh.shape
+    Skv = kh.shape[0]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    s = (qh @ kh.T) * scale
+    allowed = np.ones((Sq, Skv), dtype=bool)
+    if causal:
+        allowed &= np.arange(Skv)[None, :] <= (np.arange(Sq) + (Skv - Sq))[:, None]
+    if key_keep is not None:
+        allowed &= key_keep
+    s = np.where(allowed, s, NEG_INF)
+    mx = s.max(axis=1, keepdims=True)
+    e = np.where(allowed, np.exp(s - mx), 0.0)
+    z = e.sum(axis=1, keepdims=True)
+    p = e / z
+    return p @ vh, (mx + np.log(z))[:, 0], p
+
+
+def skipped_mass(p_dense: np.ndarray, skipped_keys: np.ndarray) -> np.ndarray:
+    """epsilon_r: dense softmax probability that row r puts on skipped keys."""
+    return (p_dense * skipped_keys).sum(axis=1)
