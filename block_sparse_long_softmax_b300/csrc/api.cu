@@ -1,0 +1,312 @@
+// C ABI of libskipsm: argument validation, tensor maps, launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/skipsm.h"
+#include "internal.h"
+
+namespace skipsm {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+skipsm_status fail(skipsm_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+skipsm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SKIPSM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- driver entry point for tensor-map encoding (no libcuda link needed)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor [Z][S][D] (D innermost) seen as 3-D with a (64 x rows x 1) box
+// and 128-byte swizzle; out-of-range elements read as zero.
+skipsm_status make_map(CUtensorMap* m, const void* base, int D, long long S, long long Z,
+                       int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(SKIPSM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SKIPSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SKIPSM_OK;
+}
+
+long long wait_cycles(int ms) {
+  if (ms <= 0) ms = 2000;
+  return static_cast<long long>(ms) * 2100000LL;  // upper SM clock, 2.1 GHz
+}
+
+skipsm_status check_lambda(float lambda) {
+  if (!std::isfinite(lambda) || lambda < 0.f || lambda > 1.f)
+    return fail(SKIPSM_ERR_INVALID_ARG, "lambda must be finite and in [0, 1] (got %g)", lambda);
+  return SKIPSM_OK;
+}
+
+void set_lambda(float lambda, float* lam_log2, int* lam_pos) {
+  *lam_pos = lambda > 0.f;
+  *lam_log2 = lambda > 0.f ? static_cast<float>(std::log2(static_cast<double>(lambda))) : -INFINITY;
+}
+
+constexpr int kDecodeBk = 64;
+constexpr int kDecodeTargetCtas = 148 * 2 * 4;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int* device_status_word() {
+  static int* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace skipsm
+
+using namespace skipsm;
+
+extern "C" {
+
+int skipsm_version(void) { return SKIPSM_VERSION; }
+
+const char* skipsm_last_error(void) { return t_last_error; }
+
+skipsm_status skipsm_check(void* stream, int* device_status) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int* w = device_status_word();
+  if (!w) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
+  int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device status");
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear device status");
+  }
+  if (device_status) *device_status = v;
+  if (v) return fail(SKIPSM_ERR_TIMEOUT, "a kernel wait exceeded its bound (site %d)", v);
+  t_last_error[0] = '\0';
+  return SKIPSM_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, void* o, int B,
+                                int Hq, int Hkv, int Sq, int Skv, int D, int causal, float lambda,
+                                uint64_t* skip_counts, const skipsm_prefill_opts* opts,
+                                void* stream) {
+  skipsm_prefill_opts op;
+  std::memset(&op, 0, sizeof(op));
+  if (opts) op = *opts;
+  if (!q || !k || !v || !o) return fail(SKIPSM_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(SKIPSM_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1)
+    return fail(SKIPSM_ERR_INVALID_ARG, "sizes must be >= 1");
+  if (Hq % Hkv) return fail(SKIPSM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  if (D != 64 && D != 128) return fail(SKIPSM_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", D);
+  if (causal && Sq > Skv) return fail(SKIPSM_ERR_INVALID_ARG, "causal prefill needs Sq <= Skv");
+  skipsm_status st = check_lambda(lambda);
+  if (st) return st;
+  const int tq = op.tile_q ? op.tile_q : (D == 64 ? 64 : 128);
+  const int tk = op.tile_k ? op.tile_k : (D == 64 ? 64 : 128);
+  if ((tq != 64 && tq != 128) || (tk != 64 && tk != 128))
+    return fail(SKIPSM_ERR_UNSUPPORTED, "tile_q / tile_k must be 64 or 128");
+  if (!(op.softmax_scale >= 0.f) || !std::isfinite(op.softmax_scale))
+    return fail(SKIPSM_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  const long long nblk_q = (Sq + 255) / 256;
+  if (nblk_q * B * Hq > 0x7FFFFFFFLL) return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
+  int* status = device_status_word();
+  if (!status) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
+
+  CUtensorMap qmap, kmap, vmap;
+  if ((st = make_map(&qmap, q, D, Sq, static_cast<long long>(B) * Hq, 128))) return st;
+  if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, tk))) return st;
+  if ((st = make_map(&vmap, v, D, Skv, static_cast<long long>(B) * Hkv, tk))) return st;
+
+  PrefillParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.tile_q = tq; p.tile_k = tk;
+  p.nqt = (Sq + tq - 1) / tq;
+  p.nkt = (Skv + tk - 1) / tk;
+  p.nblk_q = static_cast<int>(nblk_q);
+  const double scale = op.softmax_scale > 0.f ? op.softmax_scale : 1.0 / std::sqrt((double)D);
+  p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  set_lambda(lambda, &p.lam_log2, &p.lam_pos);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = op.lse;
+  p.skip_counts = reinterpret_cast<unsigned long long*>(skip_counts);
+  p.visited_counts = reinterpret_cast<unsigned long long*>(op.visited_counts);
+  p.skip_mask = op.skip_mask;
+  p.status = status;
+  p.wait_cycles = wait_cycles(op.wait_limit_ms);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (skip_counts && (e = cudaMemsetAsync(skip_counts, 0, sizeof(uint64_t) * Hq, s)))
+    return cuda_fail(e, "zero skip_counts");
+  if (op.visited_counts && (e = cudaMemsetAsync(op.visited_counts, 0, sizeof(uint64_t) * Hq, s)))
+    return cuda_fail(e, "zero visited_counts");
+  if (op.skip_mask &&
+      (e = cudaMemsetAsync(op.skip_mask, 2, static_cast<size_t>(B) * Hq * p.nqt * p.nkt, s)))
+    return cuda_fail(e, "init skip_mask");
+  if ((e = launch_prefill(qmap, kmap, vmap, p, s))) return cuda_fail(e, "prefill launch");
+  return SKIPSM_OK;
+}
+
+skipsm_status skipsm_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                             int Hkv, int Sq, int Skv, int D, int causal, float lambda,
+                             uint64_t* skip_counts, void* stream) {
+  return skipsm_prefill_ex(q, k, v, o, B, Hq, Hkv, Sq, Skv, D, causal, lambda, skip_counts,
+                           nullptr, stream);
+}
+
+// ------------------------------------------------------------------- decode
+int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested) {
+  if (B < 1 || Hkv < 1 || Skv < 1 || requested < 0) return 0;
+  const int nblk = (Skv + kDecodeBk - 1) / kDecodeBk;
+  int want = requested;
+  if (want == 0) {
+    const long long items = static_cast<long long>(B) * Hkv;
+    want = static_cast<int>((kDecodeTargetCtas + items - 1) / items);
+    want = std::min(want, std::max(1, nblk / 4));
+  }
+  want = std::max(1, std::min(want, nblk));
+  const int per = (nblk + want - 1) / want;
+  return (nblk + per - 1) / per;
+}
+
+size_t skipsm_decode_workspace_size(int B, int Hq, int Hkv, int Skv, int D, int num_splits) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv || D < 1) return 0;
+  const int ns = skipsm_decode_num_splits(B, Hkv, Skv, num_splits);
+  if (ns == 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * ns;
+  return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                               int Hkv, int Skv, int D, float lambda, uint64_t* skip_counts,
+                               void* workspace, size_t workspace_bytes,
+                               const skipsm_decode_opts* opts, void* stream) {
+  skipsm_decode_opts op;
+  std::memset(&op, 0, sizeof(op));
+  if (opts) op = *opts;
+  if (!q || !k || !v || !o) return fail(SKIPSM_ERR_INVALID_ARG, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(SKIPSM_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (B < 1 || Hq < 1 || Hkv < 1 || Skv < 1) return fail(SKIPSM_ERR_INVALID_ARG, "sizes must be >= 1");
+  if (Hq % Hkv) return fail(SKIPSM_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(SKIPSM_ERR_UNSUPPORTED, "decode GQA group %d (supported: 1, 2, 4, 8)", G);
+  if (D != 64 && D != 128) return fail(SKIPSM_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", D);
+  skipsm_status st = check_lambda(lambda);
+  if (st) return st;
+  if (op.num_splits < 0) return fail(SKIPSM_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (!(op.softmax_scale >= 0.f) || !std::isfinite(op.softmax_scale))
+    return fail(SKIPSM_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  if (static_cast<long long>(B) * Hkv > 65535LL * 65535LL)
+    return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
+  if (B > 65535 || Hkv > 65535) return fail(SKIPSM_ERR_UNSUPPORTED, "B and Hkv must be <= 65535");
+  const int ns = skipsm_decode_num_splits(B, Hkv, Skv, op.num_splits);
+  const size_t need = skipsm_decode_workspace_size(B, Hq, Hkv, Skv, D, op.num_splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(SKIPSM_ERR_WORKSPACE, "decode needs %zu bytes of workspace (got %zu)", need,
+                workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(SKIPSM_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  int* status = device_status_word();
+  if (!status) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
+
+  CUtensorMap kmap, vmap;
+  if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, kDecodeBk))) return st;
+  if ((st = make_map(&vmap, v, D, Skv, static_cast<long long>(B) * Hkv, kDecodeBk))) return st;
+
+  const int nblk = (Skv + kDecodeBk - 1) / kDecodeBk;
+  const size_t rows = static_cast<size_t>(B) * Hq * ns;
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.Skv = Skv; p.D = D;
+  p.nblk = nblk;
+  p.per = (nblk + ns - 1) / ns;
+  p.nsplit = ns;
+  const double scale = op.softmax_scale > 0.f ? op.softmax_scale : 1.0 / std::sqrt((double)D);
+  p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  set_lambda(lambda, &p.lam_log2, &p.lam_pos);
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * D * sizeof(float)));
+  p.skip_counts = reinterpret_cast<unsigned long long*>(skip_counts);
+  p.skip_mask = op.skip_mask;
+  p.status = status;
+  p.wait_cycles = wait_cycles(op.wait_limit_ms);
+  p.inject_fault = op.inject_wait_timeout ? 1 : 0;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (skip_counts && (e = cudaMemsetAsync(skip_counts, 0, sizeof(uint64_t) * Hq, s)))
+    return cuda_fail(e, "zero skip_counts");
+  if ((e = launch_decode(kmap, vmap, p, B, s))) return cuda_fail(e, "decode split launch");
+  CombineParams c;
+  c.ws_o = p.ws_o;
+  c.ws_lse = p.ws_lse;
+  c.o = static_cast<__nv_bfloat16*>(o);
+  c.lse = op.lse;
+  c.Hq = Hq; c.D = D; c.nsplit = ns;
+  if ((e = launch_combine(c, B, s))) return cuda_fail(e, "decode combine launch");
+  return SKIPSM_OK;
+}
+
+skipsm_status skipsm_decode(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                            int Hkv, int Skv, int D, float lambda, uint64_t* skip_counts,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return skipsm_decode_ex(q, k, v, o, B, Hq, Hkv, Skv, D, lambda, skip_counts, workspace,
+                          workspace_bytes, nullptr, stream);
+}
+
+}  // extern "C"

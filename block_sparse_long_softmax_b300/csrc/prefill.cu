@@ -1,0 +1,470 @@
+// Skip Softmax prefill for sm_103a (tcgen05 + TMEM + TMA).
+//
+// Attention is computed tile by tile with an online softmax; for each
+// (query tile, key tile) the tile's row maxima are compared with the running
+// row maxima and the tile is skipped — no exponentials, no P.V MMA — when every
+// row satisfies exp(local max - running max) < lambda ("Accelerating
+// Long-Context Inference with Skip Softmax in NVIDIA TensorRT-LLM", "Skip
+// Softmax Mechanism"; "NVIDIA Introduces Skip Softmax ...", "Understanding
+// Skip Softmax").  The exponential work is what a skipped tile saves on
+// Blackwell, where the exp units, not the tensor cores, bound attention
+// ("Approximating Softmax in Pretrained LLMs ...", Abstract).
+//
+// CTA = 256 query rows of one (batch, query head) = two 128-row Q tiles.
+//   warp 0      TMA producer: Q once, then K_j / V_j into 2-stage rings
+//   warp 1      TMEM allocator and MMA issuer (one thread):
+//                 S_x = Q_x K_j^T   (A, B from shared memory, D in TMEM)
+//                 O_x += P_x V_j    (A = P from TMEM, B = V from shared memory)
+//   warps 4-7   softmax of Q tile 0, warps 8-11 softmax of Q tile 1:
+//                 one thread per row = one TMEM lane; reads S, takes the row
+//                 max, votes, and for kept tiles writes bf16 P over S in TMEM
+// The two Q tiles ping-pong: while one warpgroup runs its softmax the tensor
+// core works on the other tile.  The running max used by the vote is always
+// the exact prefix max; the accumulator's reference max is only moved when the
+// max has grown by more than 2^8 (lazy rescaling), which changes no result.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace skipsm {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D, int BK, int TQ, int NS>
+struct PrefillCfg {
+  static constexpr int kQTileBytes = kQRows * D * 2;
+  static constexpr int kKVBytes = BK * D * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
+  static constexpr int kOffV = kOffK + NS * kKVBytes;
+  static constexpr int kOffBar = kOffV + NS * kKVBytes;
+  // barriers: qfull, kfull[NS], kempty[NS], vfull[NS], vempty[NS], sfull[2],
+  //           pfull[2], odone[2], final
+  static constexpr int kNBar = 1 + 4 * NS + 6 + 1;
+  static constexpr int kOffVote = kOffBar + kNBar * 8;       // [2 x][2 parity][4 warps] int
+  static constexpr int kOffDec = kOffVote + 2 * 2 * 4 * 4;   // [2] int
+  static constexpr int kOffTmem = kOffDec + 2 * 4;           // uint32
+  static constexpr int kOffAbort = kOffTmem + 4;
+  static constexpr int kBytes = kOffAbort + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  // TMEM columns: S/P of tile x at x*BK, O of tile x at 2*BK + x*D
+  static constexpr int kColS0 = 0, kColS1 = BK, kColO0 = 2 * BK, kColO1 = 2 * BK + D;
+  static constexpr int kTmemUsed = 2 * BK + 2 * D;
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256u : 512u;
+  static constexpr uint32_t kIdescQK = idesc_bf16(kQRows, BK, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kQRows, D, false, true);
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BK == 64 || BK == 128, "key tile");
+  static_assert(TQ == 64 || TQ == 128, "vote rows");
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+};
+
+__device__ __forceinline__ float gapf(float tile_max, float run_max) {
+  if (tile_max == -INFINITY) return -INFINITY;
+  if (run_max == -INFINITY) return INFINITY;
+  return tile_max - run_max;
+}
+
+// Number of key tiles visible to any query row < row_end (0 if the tile is empty).
+__device__ __forceinline__ int tiles_visible(int row_begin, int row_end, const PrefillParams& p,
+                                             int BK) {
+  if (row_begin >= p.Sq) return 0;
+  row_end = min(row_end, p.Sq);
+  if (!p.causal) return p.nkt;
+  const int last_key = min(p.Skv - 1, row_end - 1 + (p.Skv - p.Sq));
+  return last_key / BK + 1;
+}
+
+template <int D, int BK, int TQ, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  using C = PrefillCfg<D, BK, TQ, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+  const uint32_t bar0 = sbase + C::kOffBar;
+  const uint32_t qfull = bar0;
+  auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kempty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
+  auto vfull = [&](int s) { return bar0 + 8u * (1 + 2 * NS + s); };
+  auto vempty = [&](int s) { return bar0 + 8u * (1 + 3 * NS + s); };
+  auto sfull = [&](int x) { return bar0 + 8u * (1 + 4 * NS + x); };
+  auto pfull = [&](int x) { return bar0 + 8u * (3 + 4 * NS + x); };
+  auto odone = [&](int x) { return bar0 + 8u * (5 + 4 * NS + x); };
+  const uint32_t final_bar = bar0 + 8u * (7 + 4 * NS);
+  int* svote = reinterpret_cast<int*>(smem + C::kOffVote);
+  volatile int* sdec = reinterpret_cast<volatile int*>(smem + C::kOffDec);
+  uint32_t* stmem = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  const WaitCtx wc{p.wait_cycles, p.status, abort_flag};
+
+  // ---- work item: heaviest (last) query blocks first, GQA siblings adjacent
+  int id = blockIdx.x;
+  const int gi = id % p.G;
+  id /= p.G;
+  const int hkv = id % p.Hkv;
+  id /= p.Hkv;
+  const int b = id % p.B;
+  const int qblk = p.nblk_q - 1 - id / p.B;
+  const int hq = hkv * p.G + gi;
+  const int qrow0 = qblk * 2 * kQRows;
+  const int n0 = tiles_visible(qrow0, qrow0 + kQRows, p, BK);
+  const int n1 = tiles_visible(qrow0 + kQRows, qrow0 + 2 * kQRows, p, BK);
+  const int nmax = max(n0, n1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(kfull(s), 1);
+      mbar_init(kempty(s), 1);
+      mbar_init(vfull(s), 1);
+      mbar_init(vempty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(sfull(x), 1);
+      mbar_init(pfull(x), 4);
+      mbar_init(odone(x), 1);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(stmem), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *stmem;
+
+  if (warp == 0) {
+    // ================================================================ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      const int zq = b * p.Hq + hq, zk = b * p.Hkv + hkv;
+      mbar_arrive_expect_tx(qfull, 2 * C::kQTileBytes);
+      for (int x = 0; x < 2; ++x)
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull, h * 64,
+                      qrow0 + x * kQRows, zq);
+      int issued = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(kempty(s), ((j / NS) - 1) & 1, wc, kSitePrefillKEmpty)) break;
+        mbar_arrive_expect_tx(kfull(s), C::kKVBytes);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sK + s * C::kKVBytes + h * BK * 128, &kmap, kfull(s), h * 64, j * BK, zk);
+        if (j >= NS && !mbar_wait(vempty(s), ((j / NS) - 1) & 1, wc, kSitePrefillVEmpty)) {
+          issued = 2 * j + 1;
+          break;
+        }
+        mbar_arrive_expect_tx(vfull(s), C::kKVBytes);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sV + s * C::kKVBytes + h * BK * 128, &vmap, vfull(s), h * 64, j * BK, zk);
+        issued = 2 * j + 2;
+      }
+      if (*abort_flag) {
+        // let every copy in flight land before the CTA can exit
+        const long long t0 = clock64();
+        while (!mbar_try_wait(qfull, 0) && clock64() - t0 < p.wait_cycles) {}
+        const int nk = (issued + 1) / 2, nv = issued / 2;
+        for (int j = max(0, nk - NS); j < nk; ++j)
+          while (!mbar_try_wait(kfull(j % NS), (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
+        for (int j = max(0, nv - NS); j < nv; ++j)
+          while (!mbar_try_wait(vfull(j % NS), (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA
+    if (lane == 0 && nmax > 0) {
+      const int nx[2] = {n0, n1};
+      const uint32_t colS[2] = {C::kColS0, C::kColS1};
+      const uint32_t colO[2] = {C::kColO0, C::kColO1};
+      bool first_pv[2] = {true, true};
+      auto issue_s = [&](int x, int stage) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qa = sQ + x * C::kQTileBytes + (kk >> 2) * (kQRows * 128) + (kk & 3) * 32;
+          const uint32_t kb = sK + stage * C::kKVBytes + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+          umma_ss(tmem + colS[x], sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb, 16, 1024),
+                  C::kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int x, int stage) {
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t vb = sV + stage * C::kKVBytes + kk * 16 * 128;
+          umma_ts(tmem + colO[x], tmem + colS[x] + kk * 8, sdesc_sw128(vb, BK * 128, 1024),
+                  C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u);
+        }
+        first_pv[x] = false;
+      };
+      bool ok = mbar_wait(qfull, 0, wc, kSitePrefillQ) &&
+                mbar_wait(kfull(0), 0, wc, kSitePrefillKFull);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (nx[x] > 0) {
+            issue_s(x, 0);
+            umma_commit(sfull(x));
+          }
+        umma_commit(kempty(0));
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int s = j % NS, s1 = (j + 1) % NS;
+        const bool has_next = j + 1 < nmax;
+        bool v_ready = false;
+        if (has_next && !mbar_wait(kfull(s1), ((j + 1) / NS) & 1, wc, kSitePrefillKFull)) break;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (j >= nx[x]) continue;
+          if (!mbar_wait(pfull(x), j & 1, wc, kSitePrefillPFull)) { ok = false; break; }
+          tc_fence_after();
+          if (sdec[x]) {
+            if (!v_ready) {
+              if (!mbar_wait(vfull(s), (j / NS) & 1, wc, kSitePrefillVFull)) { ok = false; break; }
+              v_ready = true;
+              tc_fence_after();
+            }
+            issue_pv(x, s);
+            umma_commit(odone(x));
+          }
+          if (j + 1 < nx[x]) {
+            issue_s(x, s1);
+            umma_commit(sfull(x));
+          }
+        }
+        if (!ok) break;
+        if (has_next) umma_commit(kempty(s1));
+        if (!v_ready && !mbar_wait(vfull(s), (j / NS) & 1, wc, kSitePrefillVFull)) break;
+        umma_commit(vempty(s));
+      }
+      // every MMA issued by this thread completes before TMEM is released
+      umma_commit(final_bar);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(final_bar, 0) && clock64() - t0 < p.wait_cycles) {}
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax
+    const int x = (warp - 4) >> 2;        // Q tile
+    const int wq = warp & 3;              // TMEM lane quadrant
+    const int r = wq * 32 + lane;         // row within the Q tile
+    const int row = qrow0 + x * kQRows + r;
+    const bool valid = row < p.Sq;
+    const int qpos = row + (p.Skv - p.Sq);
+    const int n = x == 0 ? n0 : n1;
+    const int grp = TQ == 128 ? 0 : (wq >> 1);           // vote group within the Q tile
+    const int grp_row0 = qrow0 + x * kQRows + grp * TQ;  // first row of this vote group
+    const int n_grp = tiles_visible(grp_row0, grp_row0 + TQ, p, BK);
+    const int qtile = grp_row0 / TQ;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
+    const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
+    const float sl2 = p.scale_log2;
+    float M = -INFINITY, R = -INFINITY, l = 0.f;
+    int npv = 0;
+    unsigned long long n_skip = 0, n_visit = 0;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
+      __syncwarp();  // tcgen05.ld is .aligned: reconverge after the spin-wait
+      tc_fence_after();
+      const int key0 = j * BK;
+      const bool need_mask = (p.causal && key0 + BK - 1 > qpos) || key0 + BK > p.Skv;
+      // ---- pass 1: row max of the raw logits
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c0 = 0; c0 < BK; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tS + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float s = __uint_as_float(v[i]);
+          if (need_mask) {
+            const int key = key0 + c0 + i;
+            if ((p.causal && key > qpos) || key >= p.Skv) s = -INFINITY;
+          }
+          mx = fmaxf(mx, s);
+        }
+      }
+      const float mt2 = valid ? mx * sl2 : -INFINITY;
+      const float d = gapf(mt2, M);
+      const bool row_vote = !valid || d < p.lam_log2;
+      const bool warp_vote = __all_sync(0xffffffffu, row_vote);
+      volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
+      // bit 0: the warp's rows all vote skip; bit 1: this warp saw an abort
+      if (lane == 0) vote[wq] = (warp_vote ? 1 : 0) | (*abort_flag ? 2 : 0);
+      named_bar_sync(1 + x, 128);
+      const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
+      if ((v0 | v1 | v2 | v3) & 2) { ok = false; break; }  // uniform across the warpgroup
+      bool skip_g[2];
+      if (TQ == 128) {
+        skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
+      } else {
+        skip_g[0] = p.lam_pos && (v0 & v1 & 1);
+        skip_g[1] = p.lam_pos && (v2 & v3 & 1);
+      }
+      // tiles past a 64-row group's causal range are not visited by it
+      if (TQ == 64) {
+        const int g0row = qrow0 + x * kQRows;
+        if (j >= tiles_visible(g0row, g0row + 64, p, BK)) skip_g[0] = true;
+        if (j >= tiles_visible(g0row + 64, g0row + 128, p, BK)) skip_g[1] = true;
+      }
+      const bool any_kept = !(skip_g[0] && skip_g[1]);
+      const bool my_skip = skip_g[grp];
+      if (r == grp * TQ && j < n_grp) {  // one thread per vote group records it
+        ++n_visit;
+        n_skip += my_skip ? 1 : 0;
+        if (p.skip_mask)
+          p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + qtile) * p.nkt + j] =
+              my_skip ? 1 : 0;
+      }
+      if (r == 0) sdec[x] = any_kept ? 1 : 0;
+      __syncwarp();
+      if (any_kept) {
+        if (!my_skip) {
+          M = fmaxf(M, mt2);
+          float alpha = 1.f;
+          bool resc = false;
+          if (M > R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
+            resc = R != -INFINITY;
+            alpha = ex2(R - M);
+            l *= alpha;
+            R = M;
+          }
+          if (__any_sync(0xffffffffu, resc)) {
+            // O must hold every earlier P.V before it is rescaled
+            ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone) && ok;
+            __syncwarp();
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t v[32];
+              tmem_ld32(tO + c0, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(tO + c0, v);
+            }
+          }
+          // ---- pass 2: P = 2^(s*scale*log2e - R) in bf16, written over S
+          const float negR = -R;
+          float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < BK; c0 += 64) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t v[32];
+              tmem_ld32(tS + c0 + 32 * h, v);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                float s0 = __uint_as_float(v[i]), s1 = __uint_as_float(v[i + 1]);
+                if (need_mask) {
+                  const int key = key0 + c0 + 32 * h + i;
+                  if ((p.causal && key > qpos) || key >= p.Skv) s0 = -INFINITY;
+                  if ((p.causal && key + 1 > qpos) || key + 1 >= p.Skv) s1 = -INFINITY;
+                }
+                const float e0 = ex2(fmaf(s0, sl2, negR)), e1 = ex2(fmaf(s1, sl2, negR));
+                l0 += e0;
+                l1 += e1;
+                pk[16 * h + i / 2] = pack_bf16x2(e0, e1);
+              }
+            }
+            tmem_st32(tS + c0 / 2, pk);
+          }
+          l += l0 + l1;
+        } else {
+          uint32_t z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+          for (int c0 = 0; c0 < BK / 2; c0 += 32) tmem_st32(tS + c0, z);
+        }
+        ++npv;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull(x));
+    }
+    if (__all_sync(0xffffffffu, ok && n > 0 && !*abort_flag)) {  // warp-uniform: TMEM loads below
+      // ---- epilogue: O / l -> bf16, LSE
+      ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone);
+      __syncwarp();
+      tc_fence_after();
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tO + c0, v);
+        if (valid && ok) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (valid && ok && p.lse)
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row] =
+            (R + __log2f(l)) * 0.69314718055994531f;
+      if (r == grp * TQ) {
+        if (p.skip_counts && n_skip) atomicAdd(p.skip_counts + hq, n_skip);
+        if (p.visited_counts && n_visit) atomicAdd(p.visited_counts + hq, n_visit);
+      }
+    }
+  }
+
+  // ---- teardown: TMEM is freed only after every MMA and TMEM access is done
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int BK, int TQ, int NS>
+cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       const PrefillParams& p, cudaStream_t stream) {
+  using C = PrefillCfg<D, BK, TQ, NS>;
+  auto kern = prefill_kernel<D, BK, TQ, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
+  kern<<<grid, kThreads, C::kAlloc, stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, const PrefillParams& p, cudaStream_t stream) {
+#define SKIPSM_PREFILL_CASE(d, bk, tq, ns) \
+  if (p.D == d && p.tile_k == bk && p.tile_q == tq) return launch_cfg<d, bk, tq, ns>(qmap, kmap, vmap, p, stream);
+  SKIPSM_PREFILL_CASE(128, 128, 128, 2)
+  SKIPSM_PREFILL_CASE(128, 128, 64, 2)
+  SKIPSM_PREFILL_CASE(128, 64, 128, 3)
+  SKIPSM_PREFILL_CASE(128, 64, 64, 3)
+  SKIPSM_PREFILL_CASE(64, 128, 128, 3)
+  SKIPSM_PREFILL_CASE(64, 128, 64, 3)
+  SKIPSM_PREFILL_CASE(64, 64, 128, 4)
+  SKIPSM_PREFILL_CASE(64, 64, 64, 4)
+#undef SKIPSM_PREFILL_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace skipsm

@@ -1,0 +1,173 @@
+/*
+ * libskipsm — Skip Softmax block-sparse attention for NVIDIA B300 (sm_103a).
+ *
+ * The operation ("Accelerating Long-Context Inference with Skip Softmax in
+ * NVIDIA TensorRT-LLM", sections "Skip Softmax Mechanism" and "Detailed
+ * Analysis"; "NVIDIA Introduces Skip Softmax for Enhanced LLM Inference
+ * Efficiency", section "Understanding Skip Softmax"): FlashAttention-style
+ * attention over key tiles with an online softmax.  For each (query tile,
+ * key tile) visited in ascending key order, let m~_r be the tile's maximum of
+ * the scaled logits in row r and m_r the running maximum of row r over the
+ * tiles before it.  The tile is skipped — no exponentials, no P.V product —
+ * when lambda > 0 and exp(m~_r - m_r) < lambda for every valid row r.  A
+ * skipped tile cannot raise the running maximum (lambda <= 1), so the maximum
+ * stays the exact prefix maximum.  lambda = 0 is exact dense attention.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are bf16, contiguous, D innermost:
+ *      prefill  q, o : [B][Hq][Sq][D]     decode  q, o : [B][Hq][D]
+ *               k, v : [B][Hkv][Skv][D]           k, v : [B][Hkv][Skv][D]
+ *    Query head h reads kv head h / (Hq / Hkv).
+ *  - All pointers are device pointers owned by the caller, 16-byte aligned.
+ *    The library never frees them and allocates no device memory per call
+ *    (tensor maps live in kernel parameters; the decode workspace is the
+ *    caller's).
+ *  - Calls only enqueue work on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and return.  Argument errors are detected on the host
+ *    before any launch and return SKIPSM_ERR_INVALID_ARG / _UNSUPPORTED with
+ *    nothing enqueued; skipsm_last_error() gives the reason (thread-local).
+ *  - Device-side failures (a pipeline wait that exceeded its bound) set a
+ *    device status word instead of trapping; skipsm_check() reads and clears it.
+ *  - Softmax scale is 1/sqrt(D) unless an _ex call gives one.  Causal masking
+ *    is bottom-right aligned: query i sits at key position Skv - Sq + i.
+ *  - lambda must be finite and in [0, 1].
+ *  - skip_counts, when not NULL, is a device array of Hq uint64 that the call
+ *    zeroes (on `stream`) and fills: prefill — skipped (query tile, key tile)
+ *    pairs per query head, summed over batch and query tiles; decode — skipped
+ *    key tiles of each GQA group, summed over batch, repeated for each of the
+ *    group's query heads (the decode vote is over the group's G heads).
+ */
+#ifndef SKIPSM_H
+#define SKIPSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKIPSM_VERSION 100
+
+typedef enum skipsm_status {
+  SKIPSM_OK = 0,
+  SKIPSM_ERR_INVALID_ARG = 1,  /* bad pointer, shape, lambda or option */
+  SKIPSM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (D, G, tiles) */
+  SKIPSM_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  SKIPSM_ERR_TIMEOUT = 4,      /* a kernel gave up on a bounded wait */
+  SKIPSM_ERR_WORKSPACE = 5     /* decode workspace missing or too small */
+} skipsm_status;
+
+/* Library version (SKIPSM_VERSION of the build). */
+int skipsm_version(void);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* skipsm_last_error(void);
+
+/*
+ * Waits for `stream`, then reads and clears the library's device status word.
+ * *device_status (if not NULL) receives the raw word: 0 = clean, otherwise a
+ * code identifying the wait that timed out.  Returns SKIPSM_ERR_TIMEOUT when
+ * the word was set, SKIPSM_ERR_CUDA when synchronisation failed.
+ */
+skipsm_status skipsm_check(void* stream, int* device_status);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Optional controls and outputs of a prefill call; zero-initialise. */
+typedef struct skipsm_prefill_opts {
+  int tile_q;             /* rows of one skip vote: 64 or 128; 0 = 64 if D == 64 else 128 */
+  int tile_k;             /* keys per key tile: 64 or 128; 0 = 64 if D == 64 else 128 */
+  float softmax_scale;    /* 0 = 1/sqrt(D) */
+  float* lse;             /* optional out [B][Hq][Sq] fp32, natural-log LSE of the kept keys */
+  uint8_t* skip_mask;     /* optional out [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)]:
+                             0 kept, 1 skipped, 2 not visited (causal) — fully written */
+  uint64_t* visited_counts; /* optional out [Hq]: visited tile pairs per head (zeroed, filled) */
+  int wait_limit_ms;      /* bound of each pipeline wait in the kernel; 0 = 2000 ms */
+} skipsm_prefill_opts;
+
+/*
+ * Skip Softmax prefill (self-attention over a prompt).
+ *   q, k, v, o       device bf16 tensors, layouts above; o is written.
+ *   B, Hq, Hkv       batch, query heads, kv heads (Hq % Hkv == 0)
+ *   Sq, Skv          query / key lengths (>= 1; Sq <= Skv when causal)
+ *   D                head dim: 64 or 128
+ *   causal           nonzero = causal mask
+ *   lambda           skip threshold in [0, 1]
+ *   skip_counts      optional device uint64[Hq] (see above)
+ * Returns SKIPSM_OK once the work is enqueued.
+ */
+skipsm_status skipsm_prefill(const void* q, const void* k, const void* v, void* o,
+                             int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                             int causal, float lambda, uint64_t* skip_counts,
+                             void* stream);
+
+/* skipsm_prefill with tile overrides and optional outputs (opts may be NULL). */
+skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, void* o,
+                                int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                int causal, float lambda, uint64_t* skip_counts,
+                                const skipsm_prefill_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Decode (one query token per sequence, split-KV + log-sum-exp combine)      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Number of KV splits a decode call uses when the caller asks for 0: enough
+ * (b, kv head, split) work items to fill the GPU, each split at least 4 key
+ * tiles of 64.  The key range is cut into ceil(nblk/splits)-tile splits, and
+ * empty trailing splits are dropped, so the count returned here is the
+ * effective one.  Returns 0 for invalid sizes.
+ */
+int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested);
+
+/*
+ * Bytes of device workspace a decode call needs: per (b, query head, split)
+ * a D-float partial output and one float log-sum-exp, 256-byte aligned.
+ * num_splits = 0 selects the default.  Returns 0 for invalid sizes.
+ */
+size_t skipsm_decode_workspace_size(int B, int Hq, int Hkv, int Skv, int D, int num_splits);
+
+/* Optional controls and outputs of a decode call; zero-initialise. */
+typedef struct skipsm_decode_opts {
+  int num_splits;         /* 0 = skipsm_decode_num_splits(B, Hkv, Skv, 0) */
+  float softmax_scale;    /* 0 = 1/sqrt(D) */
+  float* lse;             /* optional out [B][Hq] fp32 natural-log LSE */
+  uint8_t* skip_mask;     /* optional out [B][Hkv][ceil(Skv/64)]: 0 kept, 1 skipped */
+  int wait_limit_ms;      /* bound of each pipeline wait; 0 = 2000 ms */
+  int inject_wait_timeout; /* failure-detection test hook: one split-kernel wait is made to
+                              run out (nothing arrives on its barrier); the kernels end early,
+                              outputs are undefined and skipsm_check() reports site 7 */
+} skipsm_decode_opts;
+
+/*
+ * Skip Softmax decode step with GQA.  Key tiles are 64 keys; the skip vote of
+ * a tile is over the G = Hq/Hkv query heads sharing the kv head, and a skipped
+ * tile's V rows are never read from memory.
+ *   q, o             device bf16 [B][Hq][D]
+ *   k, v             device bf16 [B][Hkv][Skv][D] (the first Skv positions are valid)
+ *   Hq/Hkv           G in {1, 2, 4, 8}
+ *   D                64 or 128
+ *   workspace        device buffer of >= skipsm_decode_workspace_size(...) bytes,
+ *                    256-byte aligned, owned by the caller, not read before written
+ * Launches a split kernel and a combine kernel on `stream`.
+ */
+skipsm_status skipsm_decode(const void* q, const void* k, const void* v, void* o,
+                            int B, int Hq, int Hkv, int Skv, int D, float lambda,
+                            uint64_t* skip_counts, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* skipsm_decode with split override and optional outputs (opts may be NULL). */
+skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void* o,
+                               int B, int Hq, int Hkv, int Skv, int D, float lambda,
+                               uint64_t* skip_counts, void* workspace, size_t workspace_bytes,
+                               const skipsm_decode_opts* opts, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKIPSM_H */
