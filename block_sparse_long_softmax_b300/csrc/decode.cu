@@ -155,7 +155,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int hA = 2 * t, hB = 2 * t + 1;
   const int G = p.G;
 
-  if (p.inject_fault && threadIdx.x == 0) mbar_wait(never_bar, 0, wc, kSiteInjected);
+  if (p.inject_fault && threadIdx.x == 0) {
+    // half the normal bound, so this wait (the injected root cause) is the one reported
+    const WaitCtx half{p.wait_cycles / 2, p.status, abort_flag};
+    mbar_wait(never_bar, 0, half, kSiteInjected);
+  }
   __syncwarp();
 
   uint32_t qf[D / 16][2];

@@ -11,19 +11,22 @@
 // ("Approximating Softmax in Pretrained LLMs ...", Abstract).
 //
 // CTA = 256 query rows of one (batch, query head) = two 128-row Q tiles.
-//   warp 0      TMA producer: Q once, then K_j / V_j into 2-stage rings
+//   warp 0      TMA producer: Q once, then K_j / V_j into rings
 //   warp 1      TMEM allocator and MMA issuer (one thread):
 //                 S_x = Q_x K_j^T   (A, B from shared memory, D in TMEM)
 //                 O_x += P_x V_j    (A = P from TMEM, B = V from shared memory)
+//   warps 2-3   idle (they only give their registers to the softmax warps)
 //   warps 4-7   softmax of Q tile 0, warps 8-11 softmax of Q tile 1:
-//                 one thread per row = one TMEM lane; reads S, takes the row
-//                 max, votes, and for kept tiles writes bf16 P over S in TMEM
+//                 one thread per row = one TMEM lane; the whole S row is read
+//                 into registers at once, the row max votes, and for kept
+//                 tiles bf16 P is written over S in TMEM
 // The two Q tiles ping-pong: while one warpgroup runs its softmax the tensor
 // core works on the other tile.  The running max used by the vote is always
 // the exact prefix max; the accumulator's reference max is only moved when the
 // max has grown by more than 2^8 (lazy rescaling), which changes no result.
 #include "internal.h"
 #include "ptx.cuh"
+#include "tmem_wide.cuh"
 
 namespace skipsm {
 namespace {
@@ -31,18 +34,22 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
 constexpr float kRescaleLog2 = 8.f;
+constexpr uint32_t kRegsLow = 56;   // warps 0-3 after setmaxnreg.dec
+constexpr uint32_t kRegsHigh = 216; // softmax warpgroups after setmaxnreg.inc
+// registers the launch must provide for the split above (checked on the host)
+constexpr int kRegPoolNeeded = static_cast<int>(kRegsLow * 128 + 2 * kRegsHigh * 128);
 
-template <int D, int BK, int TQ, int NS>
+template <int D, int BK, int TQ, int NK, int NV>
 struct PrefillCfg {
   static constexpr int kQTileBytes = kQRows * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
-  static constexpr int kOffV = kOffK + NS * kKVBytes;
-  static constexpr int kOffBar = kOffV + NS * kKVBytes;
-  // barriers: qfull, kfull[NS], kempty[NS], vfull[NS], vempty[NS], sfull[2],
+  static constexpr int kOffV = kOffK + NK * kKVBytes;
+  static constexpr int kOffBar = kOffV + NV * kKVBytes;
+  // barriers: qfull, kfull[NK], kempty[NK], vfull[NV], vempty[NV], sfull[2],
   //           pfull[2], odone[2], final
-  static constexpr int kNBar = 1 + 4 * NS + 6 + 1;
+  static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 1;
   static constexpr int kOffVote = kOffBar + kNBar * 8;       // [2 x][2 parity][4 warps] int
   static constexpr int kOffDec = kOffVote + 2 * 2 * 4 * 4;   // [2] int
   static constexpr int kOffTmem = kOffDec + 2 * 4;           // uint32
@@ -59,6 +66,7 @@ struct PrefillCfg {
   static_assert(BK == 64 || BK == 128, "key tile");
   static_assert(TQ == 64 || TQ == 128, "vote rows");
   static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ float gapf(float tile_max, float run_max) {
@@ -77,12 +85,31 @@ __device__ __forceinline__ int tiles_visible(int row_begin, int row_end, const P
   return last_key / BK + 1;
 }
 
-template <int D, int BK, int TQ, int NS>
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld<64>(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld64(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_ld<128>(uint32_t taddr, uint32_t (&r)[128]) { tmem_ld128(taddr, r); }
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_st<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_st<128>(uint32_t taddr, const uint32_t (&r)[128]) {
+  tmem_st64(taddr, *reinterpret_cast<const uint32_t(*)[64]>(&r[0]));
+  tmem_st64(taddr + 64, *reinterpret_cast<const uint32_t(*)[64]>(&r[64]));
+}
+
+template <int D, int BK, int TQ, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using C = PrefillCfg<D, BK, TQ, NS>;
+  using C = PrefillCfg<D, BK, TQ, NK, NV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -91,13 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + C::kOffBar;
   const uint32_t qfull = bar0;
   auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kempty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
-  auto vfull = [&](int s) { return bar0 + 8u * (1 + 2 * NS + s); };
-  auto vempty = [&](int s) { return bar0 + 8u * (1 + 3 * NS + s); };
-  auto sfull = [&](int x) { return bar0 + 8u * (1 + 4 * NS + x); };
-  auto pfull = [&](int x) { return bar0 + 8u * (3 + 4 * NS + x); };
-  auto odone = [&](int x) { return bar0 + 8u * (5 + 4 * NS + x); };
-  const uint32_t final_bar = bar0 + 8u * (7 + 4 * NS);
+  auto kempty = [&](int s) { return bar0 + 8u * (1 + NK + s); };
+  auto vfull = [&](int s) { return bar0 + 8u * (1 + 2 * NK + s); };
+  auto vempty = [&](int s) { return bar0 + 8u * (1 + 2 * NK + NV + s); };
+  auto sfull = [&](int x) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + x); };
+  auto pfull = [&](int x) { return bar0 + 8u * (3 + 2 * NK + 2 * NV + x); };
+  auto odone = [&](int x) { return bar0 + 8u * (5 + 2 * NK + 2 * NV + x); };
+  const uint32_t final_bar = bar0 + 8u * (7 + 2 * NK + 2 * NV);
   int* svote = reinterpret_cast<int*>(smem + C::kOffVote);
   volatile int* sdec = reinterpret_cast<volatile int*>(smem + C::kOffDec);
   uint32_t* stmem = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
@@ -121,12 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(qfull, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(kfull(s), 1);
-      mbar_init(kempty(s), 1);
-      mbar_init(vfull(s), 1);
-      mbar_init(vempty(s), 1);
-    }
+    for (int s = 0; s < NK; ++s) { mbar_init(kfull(s), 1); mbar_init(kempty(s), 1); }
+    for (int s = 0; s < NV; ++s) { mbar_init(vfull(s), 1); mbar_init(vempty(s), 1); }
     for (int x = 0; x < 2; ++x) {
       mbar_init(sfull(x), 1);
       mbar_init(pfull(x), 4);
@@ -145,9 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *stmem;
 
-  if (warp == 0) {
-    // ================================================================ TMA
-    if (lane == 0) {
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ============================================================ TMA
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
@@ -157,53 +181,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < D / 64; ++h)
           tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull, h * 64,
                       qrow0 + x * kQRows, zq);
-      int issued = 0;
+      int nk = 0, nv = 0;  // tiles issued
       for (int j = 0; j < nmax; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(kempty(s), ((j / NS) - 1) & 1, wc, kSitePrefillKEmpty)) break;
-        mbar_arrive_expect_tx(kfull(s), C::kKVBytes);
+        const int ks = j % NK;
+        if (j >= NK && !mbar_wait(kempty(ks), ((j / NK) - 1) & 1, wc, kSitePrefillKEmpty)) break;
+        mbar_arrive_expect_tx(kfull(ks), C::kKVBytes);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sK + s * C::kKVBytes + h * BK * 128, &kmap, kfull(s), h * 64, j * BK, zk);
-        if (j >= NS && !mbar_wait(vempty(s), ((j / NS) - 1) & 1, wc, kSitePrefillVEmpty)) {
-          issued = 2 * j + 1;
-          break;
-        }
-        mbar_arrive_expect_tx(vfull(s), C::kKVBytes);
+          tma_load_3d(sK + ks * C::kKVBytes + h * BK * 128, &kmap, kfull(ks), h * 64, j * BK, zk);
+        ++nk;
+        const int vs = j % NV;
+        if (j >= NV && !mbar_wait(vempty(vs), ((j / NV) - 1) & 1, wc, kSitePrefillVEmpty)) break;
+        mbar_arrive_expect_tx(vfull(vs), C::kKVBytes);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sV + s * C::kKVBytes + h * BK * 128, &vmap, vfull(s), h * 64, j * BK, zk);
-        issued = 2 * j + 2;
+          tma_load_3d(sV + vs * C::kKVBytes + h * BK * 128, &vmap, vfull(vs), h * 64, j * BK, zk);
+        ++nv;
       }
       if (*abort_flag) {
         // let every copy in flight land before the CTA can exit
         const long long t0 = clock64();
         while (!mbar_try_wait(qfull, 0) && clock64() - t0 < p.wait_cycles) {}
-        const int nk = (issued + 1) / 2, nv = issued / 2;
-        for (int j = max(0, nk - NS); j < nk; ++j)
-          while (!mbar_try_wait(kfull(j % NS), (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
-        for (int j = max(0, nv - NS); j < nv; ++j)
-          while (!mbar_try_wait(vfull(j % NS), (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
+        for (int j = max(0, nk - NK); j < nk; ++j)
+          while (!mbar_try_wait(kfull(j % NK), (j / NK) & 1) && clock64() - t0 < p.wait_cycles) {}
+        for (int j = max(0, nv - NV); j < nv; ++j)
+          while (!mbar_try_wait(vfull(j % NV), (j / NV) & 1) && clock64() - t0 < p.wait_cycles) {}
       }
-    }
-  } else if (warp == 1) {
-    // ================================================================ MMA
-    if (lane == 0 && nmax > 0) {
+    } else if (warp == 1 && lane == 0 && nmax > 0) {
+      // ============================================================ MMA
       const int nx[2] = {n0, n1};
       const uint32_t colS[2] = {C::kColS0, C::kColS1};
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
       bool first_pv[2] = {true, true};
-      auto issue_s = [&](int x, int stage) {
+      auto issue_s = [&](int x, int ks) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qa = sQ + x * C::kQTileBytes + (kk >> 2) * (kQRows * 128) + (kk & 3) * 32;
-          const uint32_t kb = sK + stage * C::kKVBytes + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+          const uint32_t kb = sK + ks * C::kKVBytes + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
           umma_ss(tmem + colS[x], sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb, 16, 1024),
                   C::kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int x, int stage) {
+      auto issue_pv = [&](int x, int vs) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t vb = sV + stage * C::kKVBytes + kk * 16 * 128;
+          const uint32_t vb = sV + vs * C::kKVBytes + kk * 16 * 128;
           umma_ts(tmem + colO[x], tmem + colS[x] + kk * 8, sdesc_sw128(vb, BK * 128, 1024),
                   C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u);
         }
@@ -221,50 +241,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(kempty(0));
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % NS, s1 = (j + 1) % NS;
+        const int vs = j % NV, ks1 = (j + 1) % NK;
         const bool has_next = j + 1 < nmax;
         bool v_ready = false;
-        if (has_next && !mbar_wait(kfull(s1), ((j + 1) / NS) & 1, wc, kSitePrefillKFull)) break;
+        if (has_next && !mbar_wait(kfull(ks1), ((j + 1) / NK) & 1, wc, kSitePrefillKFull)) break;
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= nx[x]) continue;
           if (!mbar_wait(pfull(x), j & 1, wc, kSitePrefillPFull)) { ok = false; break; }
           tc_fence_after();
           if (sdec[x]) {
             if (!v_ready) {
-              if (!mbar_wait(vfull(s), (j / NS) & 1, wc, kSitePrefillVFull)) { ok = false; break; }
+              if (!mbar_wait(vfull(vs), (j / NV) & 1, wc, kSitePrefillVFull)) { ok = false; break; }
               v_ready = true;
               tc_fence_after();
             }
-            issue_pv(x, s);
+            issue_pv(x, vs);
             umma_commit(odone(x));
           }
           if (j + 1 < nx[x]) {
-            issue_s(x, s1);
+            issue_s(x, ks1);
             umma_commit(sfull(x));
           }
         }
         if (!ok) break;
-        if (has_next) umma_commit(kempty(s1));
-        if (!v_ready && !mbar_wait(vfull(s), (j / NS) & 1, wc, kSitePrefillVFull)) break;
-        umma_commit(vempty(s));
+        if (has_next) umma_commit(kempty(ks1));
+        if (!v_ready && !mbar_wait(vfull(vs), (j / NV) & 1, wc, kSitePrefillVFull)) break;
+        umma_commit(vempty(vs));
       }
       // every MMA issued by this thread completes before TMEM is released
       umma_commit(final_bar);
       const long long t0 = clock64();
       while (!mbar_try_wait(final_bar, 0) && clock64() - t0 < p.wait_cycles) {}
     }
-  } else if (warp >= 4) {
+  } else {
     // ============================================================ softmax
+    setmaxnreg_inc<kRegsHigh>();
     const int x = (warp - 4) >> 2;        // Q tile
     const int wq = warp & 3;              // TMEM lane quadrant
     const int r = wq * 32 + lane;         // row within the Q tile
     const int row = qrow0 + x * kQRows + r;
     const bool valid = row < p.Sq;
-    const int qpos = row + (p.Skv - p.Sq);
+    const int qoff = p.Skv - p.Sq;
+    const int qpos = row + qoff;
+    const int qpos_warp0 = qrow0 + x * kQRows + wq * 32 + qoff;  // smallest position in this warp
     const int n = x == 0 ? n0 : n1;
     const int grp = TQ == 128 ? 0 : (wq >> 1);           // vote group within the Q tile
     const int grp_row0 = qrow0 + x * kQRows + grp * TQ;  // first row of this vote group
     const int n_grp = tiles_visible(grp_row0, grp_row0 + TQ, p, BK);
+    const int n_half0 = tiles_visible(qrow0 + x * kQRows, qrow0 + x * kQRows + 64, p, BK);
+    const int n_half1 = tiles_visible(qrow0 + x * kQRows + 64, qrow0 + x * kQRows + 128, p, BK);
     const int qtile = grp_row0 / TQ;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
@@ -276,26 +301,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
-      __syncwarp();  // tcgen05.ld is .aligned: reconverge after the spin-wait
       tc_fence_after();
+      uint32_t sv[BK];
+      tmem_ld<BK>(tS, sv);
       const int key0 = j * BK;
-      const bool need_mask = (p.causal && key0 + BK - 1 > qpos) || key0 + BK > p.Skv;
-      // ---- pass 1: row max of the raw logits
-      float mx = -INFINITY;
+      // tile-level (warp-uniform) test: does any row of this warp see a masked key?
+      if ((p.causal && key0 + BK - 1 > qpos_warp0) || key0 + BK > p.Skv) {
 #pragma unroll
-      for (int c0 = 0; c0 < BK; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tS + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float s = __uint_as_float(v[i]);
-          if (need_mask) {
-            const int key = key0 + c0 + i;
-            if ((p.causal && key > qpos) || key >= p.Skv) s = -INFINITY;
-          }
-          mx = fmaxf(mx, s);
+        for (int i = 0; i < BK; ++i) {
+          const int key = key0 + i;
+          const bool masked = (p.causal && key > qpos) || key >= p.Skv;
+          sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
         }
       }
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sv[k]);
+#pragma unroll
+      for (int i = 8; i < BK; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], __uint_as_float(sv[i + k]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mt2 = valid ? mx * sl2 : -INFINITY;
       const float d = gapf(mt2, M);
       const bool row_vote = !valid || d < p.lam_log2;
@@ -310,14 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (TQ == 128) {
         skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
       } else {
-        skip_g[0] = p.lam_pos && (v0 & v1 & 1);
-        skip_g[1] = p.lam_pos && (v2 & v3 & 1);
-      }
-      // tiles past a 64-row group's causal range are not visited by it
-      if (TQ == 64) {
-        const int g0row = qrow0 + x * kQRows;
-        if (j >= tiles_visible(g0row, g0row + 64, p, BK)) skip_g[0] = true;
-        if (j >= tiles_visible(g0row + 64, g0row + 128, p, BK)) skip_g[1] = true;
+        // tiles past a 64-row group's causal range are not visited by it
+        skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= n_half0;
+        skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= n_half1;
       }
       const bool any_kept = !(skip_g[0] && skip_g[1]);
       const bool my_skip = skip_g[grp];
@@ -329,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               my_skip ? 1 : 0;
       }
       if (r == 0) sdec[x] = any_kept ? 1 : 0;
-      __syncwarp();
       if (any_kept) {
         if (!my_skip) {
           M = fmaxf(M, mt2);
@@ -344,50 +365,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (__any_sync(0xffffffffu, resc)) {
             // O must hold every earlier P.V before it is rescaled
             ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone) && ok;
-            __syncwarp();
             tc_fence_after();
-#pragma unroll
+            // 32 columns at a time: the S row is still live in registers
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t v[32];
-              tmem_ld32(tO + c0, v);
+              uint32_t ov[32];
+              tmem_ld32(tO + c0, ov);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(tO + c0, v);
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c0, ov);
             }
           }
-          // ---- pass 2: P = 2^(s*scale*log2e - R) in bf16, written over S
+          // P = 2^(s*scale*log2e - R) in bf16, written over S
           const float negR = -R;
-          float l0 = 0.f, l1 = 0.f;
+          float la[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[BK / 2];
 #pragma unroll
-          for (int c0 = 0; c0 < BK; c0 += 64) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t v[32];
-              tmem_ld32(tS + c0 + 32 * h, v);
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                float s0 = __uint_as_float(v[i]), s1 = __uint_as_float(v[i + 1]);
-                if (need_mask) {
-                  const int key = key0 + c0 + 32 * h + i;
-                  if ((p.causal && key > qpos) || key >= p.Skv) s0 = -INFINITY;
-                  if ((p.causal && key + 1 > qpos) || key + 1 >= p.Skv) s1 = -INFINITY;
-                }
-                const float e0 = ex2(fmaf(s0, sl2, negR)), e1 = ex2(fmaf(s1, sl2, negR));
-                l0 += e0;
-                l1 += e1;
-                pk[16 * h + i / 2] = pack_bf16x2(e0, e1);
-              }
-            }
-            tmem_st32(tS + c0 / 2, pk);
+          for (int i = 0; i < BK / 2; ++i) {
+            const float e0 = ex2(fmaf(__uint_as_float(sv[2 * i]), sl2, negR));
+            const float e1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), sl2, negR));
+            la[i & 3] += e0 + e1;
+            pk[i] = pack_bf16x2(e0, e1);
           }
-          l += l0 + l1;
+          l += (la[0] + la[1]) + (la[2] + la[3]);
+          tmem_st<BK / 2>(tS, pk);
         } else {
-          uint32_t z[32];
+          uint32_t z[BK / 2];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-          for (int c0 = 0; c0 < BK / 2; c0 += 32) tmem_st32(tS + c0, z);
+          for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
+          tmem_st<BK / 2>(tS, z);
         }
         ++npv;
       }
@@ -398,28 +404,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__all_sync(0xffffffffu, ok && n > 0 && !*abort_flag)) {  // warp-uniform: TMEM loads below
       // ---- epilogue: O / l -> bf16, LSE
       ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone);
-      __syncwarp();
       tc_fence_after();
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row) * D;
+      uint32_t ov[D];
+      tmem_ld<D>(tO, ov);
+      if (valid && ok) {
+        const float inv = 1.f / l;
+        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row) * D;
+        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tO + c0, v);
-        if (valid && ok) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        for (int i = 0; i < D / 8; ++i)
+          dst[i] = make_uint4(
+              pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
+        if (p.lse)
+          p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row] =
+              (R + __log2f(l)) * 0.69314718055994531f;
       }
-      if (valid && ok && p.lse)
-        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row] =
-            (R + __log2f(l)) * 0.69314718055994531f;
       if (r == grp * TQ) {
         if (p.skip_counts && n_skip) atomicAdd(p.skip_counts + hq, n_skip);
         if (p.visited_counts && n_visit) atomicAdd(p.visited_counts + hq, n_visit);
@@ -437,12 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK, int TQ, int NS>
+template <int D, int BK, int TQ, int NK, int NV>
 cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const PrefillParams& p, cudaStream_t stream) {
-  using C = PrefillCfg<D, BK, TQ, NS>;
-  auto kern = prefill_kernel<D, BK, TQ, NS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+  using C = PrefillCfg<D, BK, TQ, NK, NV>;
+  auto kern = prefill_kernel<D, BK, TQ, NK, NV>;
+  // setmaxnreg moves registers inside the CTA's launch allocation: refuse to
+  // launch (instead of letting .inc wait forever) if that pool is too small.
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kThreads < kRegPoolNeeded) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
   kern<<<grid, kThreads, C::kAlloc, stream>>>(qmap, kmap, vmap, p);
@@ -453,16 +461,17 @@ cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const C
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillParams& p, cudaStream_t stream) {
-#define SKIPSM_PREFILL_CASE(d, bk, tq, ns) \
-  if (p.D == d && p.tile_k == bk && p.tile_q == tq) return launch_cfg<d, bk, tq, ns>(qmap, kmap, vmap, p, stream);
-  SKIPSM_PREFILL_CASE(128, 128, 128, 2)
-  SKIPSM_PREFILL_CASE(128, 128, 64, 2)
-  SKIPSM_PREFILL_CASE(128, 64, 128, 3)
-  SKIPSM_PREFILL_CASE(128, 64, 64, 3)
-  SKIPSM_PREFILL_CASE(64, 128, 128, 3)
-  SKIPSM_PREFILL_CASE(64, 128, 64, 3)
-  SKIPSM_PREFILL_CASE(64, 64, 128, 4)
-  SKIPSM_PREFILL_CASE(64, 64, 64, 4)
+#define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)        \
+  if (p.D == d && p.tile_k == bk && p.tile_q == tq) \
+    return launch_cfg<d, bk, tq, nk, nv>(qmap, kmap, vmap, p, stream);
+  SKIPSM_PREFILL_CASE(128, 128, 128, 3, 2)
+  SKIPSM_PREFILL_CASE(128, 128, 64, 3, 2)
+  SKIPSM_PREFILL_CASE(128, 64, 128, 4, 4)
+  SKIPSM_PREFILL_CASE(128, 64, 64, 4, 4)
+  SKIPSM_PREFILL_CASE(64, 128, 128, 4, 3)
+  SKIPSM_PREFILL_CASE(64, 128, 64, 4, 3)
+  SKIPSM_PREFILL_CASE(64, 64, 128, 6, 6)
+  SKIPSM_PREFILL_CASE(64, 64, 64, 6, 6)
 #undef SKIPSM_PREFILL_CASE
   return cudaErrorInvalidValue;
 }

@@ -1,0 +1,83 @@
+"""bench.py host logic: timing harness (1 and 2 gloo ranks) and workload arithmetic."""
+
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import synth
+
+
+def test_dense_flops_of_the_128k_prefill():
+    w = synth.WORKLOADS["prefill_128k_gqa8"]
+    assert bench.prefill_dense_flops(w) == 4.0 * 64 * 128 * (131072 * 131073 // 2)
+    assert abs(bench.prefill_dense_flops(w) - 2.8147e14) / 2.8147e14 < 1e-3
+    w0 = synth.WORKLOADS["prefill_1k_d64"]
+    assert bench.prefill_dense_flops(w0) == 4.0 * 64 * (1024 * 1025 // 2)
+    wn = w0.with_(causal=False, Sq=100, Skv=300)
+    assert bench.prefill_dense_flops(wn) == 4.0 * 64 * 100 * 300
+    wc = w0.with_(Sq=100, Skv=300)  # bottom-right aligned: query i sees 201 + i keys
+    assert bench.prefill_dense_flops(wc) == 4.0 * 64 * sum(201 + i for i in range(100))
+
+
+def test_exec_flops_and_decode_bytes():
+    w = synth.WORKLOADS["prefill_128k_gqa8"]
+    per = 2 * 128 * 128 * 128
+    assert bench.prefill_exec_flops(w, 10, 4, 128, 128) == per * 10 + per * 6
+    wd = synth.WORKLOADS["decode_128k_gqa8"]
+    nblk = 8 * 8 * 2048
+    dense = bench.decode_bytes(wd, nblk, 16)
+    k_bytes = 8 * 8 * 131072 * 128 * 2
+    assert dense > 2 * k_bytes and dense < 2 * k_bytes * 1.01
+    assert bench.decode_bytes(wd, 0, 16) < 0.51 * dense
+
+
+def test_timed_loop_single_process():
+    calls = []
+    sec, wall = bench.timed_loop(lambda i: calls.append(i), 4, 3, lambda: None, lambda: 1.25,
+                                 False)
+    assert calls == [0, 1, 2, 0, 1, 2, 3]
+    assert sec == 1.25 and wall >= 0
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    steps = []
+    sec, _ = bench.timed_loop(lambda i: steps.append(i), 5, 3, lambda: None,
+                              lambda: 1.0 + rank, True)
+    ws, r, lr = bench.dist_env()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"sec": sec, "steps": len(steps), "env": [ws, r, lr]}, f)
+    dist.destroy_process_group()
+
+
+def test_timed_loop_two_gloo_ranks_take_the_max(tmp_path):
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True,
+                       start_method="spawn")
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(2)]
+    for r, d in enumerate(res):
+        assert d["sec"] == 2.0           # max over ranks of (1 + rank)
+        assert d["steps"] == 8           # warm-up + timed
+        assert d["env"] == [2, r, r]
+
+
+def test_reference_arm_non_zero_rank_exits_quietly(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out == ""
