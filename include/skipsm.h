@@ -166,6 +166,39 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
                                uint64_t* skip_counts, void* workspace, size_t workspace_bytes,
                                const skipsm_decode_opts* opts, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Decode without a caller-provided workspace                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device memory the library keeps for skipsm_decode_noalloc. */
+#define SKIPSM_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * skipsm_decode for callers that cannot allocate device memory — for example a
+ * plugin running inside a host framework that owns every device allocation, or
+ * a serving loop that must never call cudaMalloc (it can synchronise the device).
+ * The Skip Softmax pages have no counterpart of this call: it changes only where
+ * the split-KV partial results are kept.
+ *
+ * Arguments, layouts, results and errors are those of skipsm_decode with the
+ * default number of splits, minus the workspace.  The partials live in one
+ * SKIPSM_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB) array of device memory owned by
+ * the library; every GPU that loads the library holds it until the process
+ * exits.  A shape whose workspace, skipsm_decode_workspace_size(B, Hq, Hkv,
+ * Skv, D, 0), is larger than that is rejected with SKIPSM_ERR_WORKSPACE
+ * (skipsm_last_error() names the bytes needed) and nothing is launched.
+ * Nothing is allocated or freed by the call.
+ *
+ * All calls share the array and it keeps what the last call left in it; no
+ * part of it needs to start at zero.  Calls that can overlap on the GPU (other
+ * streams, other host threads) race on it: the caller must order them.  The
+ * first call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture on the device.
+ */
+skipsm_status skipsm_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                    int B, int Hq, int Hkv, int Skv, int D, float lambda,
+                                    uint64_t* skip_counts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
