@@ -11,11 +11,12 @@
 // ("Approximating Softmax in Pretrained LLMs ...", Abstract).
 //
 // CTA = 256 query rows of one (batch, query head) = two 128-row Q tiles.
-//   warp 0      TMA producer: Q once, then K_j / V_j into rings
+//   warp 0      TMA producer of Q (once) and the K_j ring
+//   warp 2      TMA producer of the V_j ring (decoupled from the K ring)
 //   warp 1      TMEM allocator and MMA issuer (one thread):
 //                 S_x = Q_x K_j^T   (A, B from shared memory, D in TMEM)
 //                 O_x += P_x V_j    (A = P from TMEM, B = V from shared memory)
-//   warps 2-3   idle (they only give their registers to the softmax warps)
+//   warp 3      idle (it only gives its registers to the softmax warps)
 //   warps 4-7   softmax of Q tile 0, warps 8-11 softmax of Q tile 1:
 //                 one thread per row = one TMEM lane; the whole S row is read
 //                 into registers at once, the row max votes, and for kept
@@ -170,40 +171,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<kRegsLow>();
-    if (warp == 0 && lane == 0) {
+    if ((warp == 0 || warp == 2) && lane == 0) {
       // ============================================================ TMA
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      const int zq = b * p.Hq + hq, zk = b * p.Hkv + hkv;
-      mbar_arrive_expect_tx(qfull, 2 * C::kQTileBytes);
-      for (int x = 0; x < 2; ++x)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull, h * 64,
-                      qrow0 + x * kQRows, zq);
-      int nk = 0, nv = 0;  // tiles issued
+      // warp 0: Q, then the K ring; warp 2: the V ring.  The two rings advance
+      // independently, so a late V tile never holds back the next K tile.
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      const int NS = is_k ? NK : NV;
+      const uint32_t ring = is_k ? sK : sV;
+      tma_prefetch_desc(map);
+      const int zk = b * p.Hkv + hkv;
+      if (is_k) {
+        tma_prefetch_desc(&qmap);
+        const int zq = b * p.Hq + hq;
+        mbar_arrive_expect_tx(qfull, 2 * C::kQTileBytes);
+        for (int x = 0; x < 2; ++x)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull, h * 64,
+                        qrow0 + x * kQRows, zq);
+      }
+      int issued = 0;
       for (int j = 0; j < nmax; ++j) {
-        const int ks = j % NK;
-        if (j >= NK && !mbar_wait(kempty(ks), ((j / NK) - 1) & 1, wc, kSitePrefillKEmpty)) break;
-        mbar_arrive_expect_tx(kfull(ks), C::kKVBytes);
+        const int st = j % NS;
+        const uint32_t empty = is_k ? kempty(st) : vempty(st);
+        const uint32_t full = is_k ? kfull(st) : vfull(st);
+        if (j >= NS && !mbar_wait(empty, ((j / NS) - 1) & 1, wc,
+                                  is_k ? kSitePrefillKEmpty : kSitePrefillVEmpty))
+          break;
+        mbar_arrive_expect_tx(full, C::kKVBytes);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sK + ks * C::kKVBytes + h * BK * 128, &kmap, kfull(ks), h * 64, j * BK, zk);
-        ++nk;
-        const int vs = j % NV;
-        if (j >= NV && !mbar_wait(vempty(vs), ((j / NV) - 1) & 1, wc, kSitePrefillVEmpty)) break;
-        mbar_arrive_expect_tx(vfull(vs), C::kKVBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sV + vs * C::kKVBytes + h * BK * 128, &vmap, vfull(vs), h * 64, j * BK, zk);
-        ++nv;
+          tma_load_3d(ring + st * C::kKVBytes + h * BK * 128, map, full, h * 64, j * BK, zk);
+        ++issued;
       }
       if (*abort_flag) {
-        // let every copy in flight land before the CTA can exit
+        // let every copy this thread started land before the CTA can exit
         const long long t0 = clock64();
-        while (!mbar_try_wait(qfull, 0) && clock64() - t0 < p.wait_cycles) {}
-        for (int j = max(0, nk - NK); j < nk; ++j)
-          while (!mbar_try_wait(kfull(j % NK), (j / NK) & 1) && clock64() - t0 < p.wait_cycles) {}
-        for (int j = max(0, nv - NV); j < nv; ++j)
-          while (!mbar_try_wait(vfull(j % NV), (j / NV) & 1) && clock64() - t0 < p.wait_cycles) {}
+        if (is_k)
+          while (!mbar_try_wait(qfull, 0) && clock64() - t0 < p.wait_cycles) {}
+        for (int j = max(0, issued - NS); j < issued; ++j) {
+          const uint32_t full = is_k ? kfull(j % NS) : vfull(j % NS);
+          while (!mbar_try_wait(full, (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
+        }
       }
     } else if (warp == 1 && lane == 0 && nmax > 0) {
       // ============================================================ MMA
@@ -314,32 +322,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
         }
       }
-      float mx8[8];
+      // 16 independent max chains, then a tree (short dependency chains)
+      float m16[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sv[k]);
+      for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
 #pragma unroll
-      for (int i = 8; i < BK; i += 8)
+      for (int i = 16; i < BK; i += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], __uint_as_float(sv[i + k]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
+      const float mx = m16[0];
       const float mt2 = valid ? mx * sl2 : -INFINITY;
       const float d = gapf(mt2, M);
       const bool row_vote = !valid || d < p.lam_log2;
       const bool warp_vote = __all_sync(0xffffffffu, row_vote);
       volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
-      // bit 0: the warp's rows all vote skip; bit 1: this warp saw an abort
-      if (lane == 0) vote[wq] = (warp_vote ? 1 : 0) | (*abort_flag ? 2 : 0);
-      named_bar_sync(1 + x, 128);
-      const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
-      if ((v0 | v1 | v2 | v3) & 2) { ok = false; break; }  // uniform across the warpgroup
+      if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
+      // A warp with a row that keeps the tile knows its vote group keeps it, so it
+      // only arrives on the barrier; warps whose rows all vote skip wait for every
+      // vote.  A 64-row group past its causal range never keeps the tile.  Every
+      // warp does exactly one barrier operation per tile, so the warps of a
+      // warpgroup stay matched even when a bounded wait has given up.
+      const bool out_of_range = TQ == 64 && j >= (grp == 0 ? n_half0 : n_half1);
       bool skip_g[2];
-      if (TQ == 128) {
-        skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
+      if ((!warp_vote || !p.lam_pos) && !out_of_range) {
+        named_bar_arrive(1 + x, 128);
+        skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
+        skip_g[grp] = false;
       } else {
-        // tiles past a 64-row group's causal range are not visited by it
-        skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= n_half0;
-        skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= n_half1;
+        named_bar_sync(1 + x, 128);
+        const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
+        if (TQ == 128) {
+          skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
+        } else {
+          // tiles past a 64-row group's causal range are not visited by it
+          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= n_half0;
+          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= n_half1;
+        }
       }
       const bool any_kept = !(skip_g[0] && skip_g[1]);
       const bool my_skip = skip_g[grp];
