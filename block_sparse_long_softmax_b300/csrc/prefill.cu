@@ -251,8 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < nmax; ++j) {
         const int vs = j % NV, ks1 = (j + 1) % NK;
         const bool has_next = j + 1 < nmax;
-        bool v_ready = false;
-        if (has_next && !mbar_wait(kfull(ks1), ((j + 1) / NK) & 1, wc, kSitePrefillKFull)) break;
+        bool v_ready = false, k_ready = false;
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= nx[x]) continue;
           if (!mbar_wait(pfull(x), j & 1, wc, kSitePrefillPFull)) { ok = false; break; }
@@ -264,11 +263,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
             }
             issue_pv(x, vs);
-            umma_commit(odone(x));
           }
           if (j + 1 < nx[x]) {
+            if (!k_ready) {  // K_{j+1} is first needed here, after P.V of tile j is queued
+              if (!mbar_wait(kfull(ks1), ((j + 1) / NK) & 1, wc, kSitePrefillKFull)) { ok = false; break; }
+              k_ready = true;
+              tc_fence_after();
+            }
             issue_s(x, ks1);
             umma_commit(sfull(x));
+          } else {
+            // the last tile of this Q tile: one commit lets the epilogue wait for its final P.V
+            umma_commit(odone(x));
           }
         }
         if (!ok) break;
@@ -304,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
     const float sl2 = p.scale_log2;
     float M = -INFINITY, R = -INFINITY, l = 0.f;
-    int npv = 0;
     unsigned long long n_skip = 0, n_visit = 0;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -385,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             R = M;
           }
           if (__any_sync(0xffffffffu, resc)) {
-            // O must hold every earlier P.V before it is rescaled
-            ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone) && ok;
-            tc_fence_after();
+            // Every earlier P.V of this Q tile is complete: the S of this tile was
+            // committed after it, and the next P.V waits for this warpgroup.
+
             // 32 columns at a time: the S row is still live in registers
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -417,15 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
           tmem_st<BK / 2>(tS, z);
         }
-        ++npv;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(pfull(x));
     }
     if (__all_sync(0xffffffffu, ok && n > 0 && !*abort_flag)) {  // warp-uniform: TMEM loads below
-      // ---- epilogue: O / l -> bf16, LSE
-      ok = mbar_wait(odone(x), (npv - 1) & 1, wc, kSitePrefillODone);
+      // ---- epilogue: O / l -> bf16, LSE (one commit after the last P.V of this Q tile)
+      ok = mbar_wait(odone(x), 0, wc, kSitePrefillODone);
       tc_fence_after();
       uint32_t ov[D];
       tmem_ld<D>(tO, ov);
