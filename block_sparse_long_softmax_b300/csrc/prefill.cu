@@ -132,14 +132,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   const WaitCtx wc{p.wait_cycles, p.status, abort_flag};
 
-  // ---- work item: heaviest (last) query blocks first, GQA siblings adjacent
+  // ---- work item.  All CTAs of one (batch, kv head) are adjacent, GQA siblings
+  // fastest and the heaviest (last) query blocks first: the CTAs resident at any
+  // time then stream the same K/V, which stays in L2 while they run.
   int id = blockIdx.x;
   const int gi = id % p.G;
   id /= p.G;
+  const int qblk = p.nblk_q - 1 - id % p.nblk_q;
+  id /= p.nblk_q;
   const int hkv = id % p.Hkv;
-  id /= p.Hkv;
-  const int b = id % p.B;
-  const int qblk = p.nblk_q - 1 - id / p.B;
+  const int b = id / p.Hkv;
   const int hq = hkv * p.G + gi;
   const int qrow0 = qblk * 2 * kQRows;
   const int n0 = tiles_visible(qrow0, qrow0 + kQRows, p, BK);
