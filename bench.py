@@ -200,11 +200,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(units_this_launch: float):
-    """DRAM bytes per prefill launch from the committed ncu summary, scaled to this launch.
+def profiled_traffic(workload: str):
+    """DRAM bytes (read + write) of one prefill launch of `workload`, from the committed
+    ncu summary, or None.
 
-    The summary records the kernel-source hash it was taken on; if the kernel
-    changed since, the counters no longer apply and this returns None.
+    The summary records the hash of the kernel source it was captured on; once the
+    kernel has changed, the counters no longer apply and this returns None.
     """
     p = os.path.join(ROOT, "profiles", "prefill_dram_traffic.txt")
     if not os.path.exists(p):
@@ -214,13 +215,12 @@ def profiled_traffic(units_this_launch: float):
         if ":" in line and not line.startswith("#"):
             a, b = line.split(":", 1)
             kv[a.strip()] = b.strip()
-    if kv.get("kernel_source_sha") != kernel_source_hash():
+    if kv.get("kernel_source_sha") != kernel_source_hash() or kv.get("workload") != workload:
         return None
     try:
-        per_unit = float(kv["dram_bytes_per_visited_tile"])
+        return float(kv["dram_bytes_read_per_launch"]) + float(kv["dram_bytes_write_per_launch"])
     except (KeyError, ValueError):
         return None
-    return per_unit * units_this_launch
 
 
 # ---------------------------------------------------------------------------
@@ -273,9 +273,9 @@ def oracle_sample(budget_s: float, lam_pf: float, lam_dec: float, splits: int, s
         r0 = t * 128
         flops += 4.0 * wp.D * sum(r + 1 for r in range(r0, r0 + 128))
         tiles.append(t)
-        t -= 13
+        t -= 7
     desc = (f"fp64 oracle: decode group (b=0, kv head 0, {wd.Skv} keys, {splits} splits) + "
-            f"{len(tiles)} query tiles of prefill head {h} (tiles {tiles[0]}..{tiles[-1]} step 13, "
+            f"{len(tiles)} query tiles of prefill head {h} (tiles {tiles[0]}..{tiles[-1]} step 7, "
             f"{wp.Skv}-key cache); dense-equivalent FLOPs of the sample / oracle seconds")
     return flops, sec, desc
 
@@ -507,7 +507,7 @@ def run_ours(args):
     achieved = exec_flops / t_pf / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(visited),
+                "frac": achieved / peak, "traffic": profiled_traffic(PREFILL),
                 "kernel": "prefill_kernel<128,128,128,2>",
                 "peak_source": f"{src} bf16_tflops_sustained (cuBLAS, power-capped loop)",
                 "burst_peak": peaks.get("bf16_tflops"),
@@ -581,6 +581,55 @@ def run_kernel_only(args):
     return 0 if status == 0 else 1
 
 
+def run_configs(args):
+    """Every configuration of the workload table at each of its lambda values (device time)."""
+    import torch
+    import block_sparse_long_softmax_b300 as bs
+    import synth
+    from synth import device as sdev
+
+    rows = []
+    for name, w in synth.WORKLOADS.items():
+        q, k, v, _ = sdev.make_inputs(w)
+        torch.cuda.synchronize()
+        for lam in w.lambdas:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(5)]
+            if w.kind == "prefill":
+                fn = lambda: bs.prefill(q, k, v, lam, causal=w.causal, tile_q=w.tile_q,  # noqa: E731
+                                        tile_k=w.tile_k, return_visited=True)
+            else:
+                fn = lambda: bs.decode(q, k, v, lam)  # noqa: E731
+            out = fn()
+            torch.cuda.synchronize()
+            for a, b in ev:
+                a.record()
+                out = fn()
+                b.record()
+            torch.cuda.synchronize()
+            sec = statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
+            if w.kind == "prefill":
+                vis = int(out.visited_counts.sum().item())
+                sk = int(out.skip_counts.sum().item())
+                rows.append({"workload": name, "lambda": lam, "ms": sec * 1e3,
+                             "skip_ratio": sk / vis,
+                             "dense_equiv_tflops": prefill_dense_flops(w) / sec / 1e12,
+                             "executed_tflops": prefill_exec_flops(w, vis, sk, w.tile_q, w.tile_k)
+                             / sec / 1e12})
+            else:
+                nblk = w.B * w.Hkv * (-(-w.Skv // 64))
+                kept = nblk - int(out.skip_counts[:: w.G].sum().item())
+                rows.append({"workload": name, "lambda": lam, "us": sec * 1e6,
+                             "skip_ratio": 1 - kept / nblk, "splits": out.num_splits,
+                             "hbm_gbs_on_bytes_read": decode_bytes(w, kept, out.num_splits)
+                             / sec / 1e9})
+        del q, k, v
+        torch.cuda.empty_cache()
+    for r in rows:
+        print(json.dumps(r), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -597,7 +646,11 @@ def main(argv=None):
     ap.add_argument("--workload", default=PREFILL)
     ap.add_argument("--lam", type=float, default=1e-3)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload configuration at each of its lambda values")
     args = ap.parse_args(argv)
+    if args.configs:
+        return run_configs(args)
     if args.kernel_only:
         return run_kernel_only(args)
     if args.warmup < 3 and args.impl == "ours":
