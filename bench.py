@@ -357,18 +357,9 @@ def run_ours(args):
         run_decode(lam)
         return int(cntd[:: wd.G].sum().item()) / nblk_d
 
-    def calibrate(fn, target):
-        lo, hi = -9.0, 0.0  # log10 lambda
-        for _ in range(14):
-            mid = 0.5 * (lo + hi)
-            if fn(10 ** mid) < target:
-                lo = mid
-            else:
-                hi = mid
-        return 10 ** (0.5 * (lo + hi))
-
-    lam_pf = {r: calibrate(prefill_rho, r) for r in SWEEP_RHO}
-    lam_dec = calibrate(decode_rho, TARGET_RHO)
+    # lambda for each target skip ratio, found by the library's calibration (bisection)
+    lam_pf = {r: bs.calibrate_prefill(q, k, v, r, out=o)[0] for r in SWEEP_RHO}
+    lam_dec = bs.calibrate_decode(qd, kd, vd, TARGET_RHO, workspace=wsp, out=od)[0]
 
     def time_events(fn, reps):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -18,7 +18,8 @@ from dataclasses import dataclass
 from typing import Optional
 
 __all__ = ["prefill", "decode", "check", "decode_num_splits", "decode_workspace_size",
-           "library", "SkipsmError", "PrefillOut", "DecodeOut", "LIB_PATH"]
+           "calibrate_prefill", "calibrate_decode", "library", "SkipsmError", "PrefillOut",
+           "DecodeOut", "Calibration", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libskipsm.so")
 
@@ -42,6 +43,11 @@ class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("lse", ctypes.c_void_p), ("skip_mask", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("inject_wait_timeout", ctypes.c_int)]
+
+
+class Calibration(ctypes.Structure):
+    _fields_ = [("lambda_", ctypes.c_float), ("skip_ratio", ctypes.c_float),
+                ("launches", ctypes.c_int)]
 
 
 _lib = None
@@ -76,6 +82,13 @@ def library() -> ctypes.CDLL:
         lib.skipsm_decode_ex.argtypes = [_P, _P, _P, _P] + [_I] * 5 + \
             [ctypes.c_float, _P, _P, ctypes.c_size_t, ctypes.POINTER(DecodeOpts), _P]
         lib.skipsm_decode_ex.restype = _I
+        lib.skipsm_prefill_calibrate.argtypes = [_P, _P, _P, _P] + [_I] * 7 + \
+            [ctypes.c_float, _I, _P, ctypes.POINTER(PrefillOpts), ctypes.POINTER(Calibration), _P]
+        lib.skipsm_prefill_calibrate.restype = _I
+        lib.skipsm_decode_calibrate.argtypes = [_P, _P, _P, _P] + [_I] * 5 + \
+            [ctypes.c_float, _I, _P, _P, ctypes.c_size_t, ctypes.POINTER(DecodeOpts),
+             ctypes.POINTER(Calibration), _P]
+        lib.skipsm_decode_calibrate.restype = _I
         _lib = lib
     return _lib
 
@@ -189,3 +202,52 @@ def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0
                                 ptr(cnt), ptr(ws), ws.numel() * ws.element_size(),
                                 ctypes.byref(opts), _P(_stream(stream))))
     return DecodeOut(o, cnt, ns, lse, mask)
+
+
+def calibrate_prefill(q, k, v, target_skip_ratio: float, causal: bool = True, *, tile_q: int = 0,
+                      tile_k: int = 0, max_iters: int = 0, out=None, stream=None):
+    """lambda whose measured prefill tile skip ratio is closest to the target.
+
+    Returns (lambda, skip_ratio, launches).  Runs the kernel max_iters times (default 14).
+    """
+    import torch
+    lib = library()
+    _check_tensor("q", q, 4), _check_tensor("k", k, 4), _check_tensor("v", v, 4)
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    counts = torch.empty(2 * Hq, dtype=torch.int64, device=q.device)
+    opts = PrefillOpts(tile_q, tile_k, 0.0, None, None, None, 0)
+    res = Calibration()
+    _raise(lib.skipsm_prefill_calibrate(_P(q.data_ptr()), _P(k.data_ptr()), _P(v.data_ptr()),
+                                        _P(o.data_ptr()), B, Hq, Hkv, Sq, Skv, D,
+                                        1 if causal else 0, float(target_skip_ratio),
+                                        int(max_iters), _P(counts.data_ptr()), ctypes.byref(opts),
+                                        ctypes.byref(res), _P(_stream(stream))))
+    return res.lambda_, res.skip_ratio, res.launches
+
+
+def calibrate_decode(q, k, v, target_skip_ratio: float, *, num_splits: int = 0,
+                     max_iters: int = 0, workspace=None, out=None, stream=None):
+    """lambda whose measured decode tile skip ratio is closest to the target.
+
+    Returns (lambda, skip_ratio, launches).
+    """
+    import torch
+    lib = library()
+    _check_tensor("q", q, 3), _check_tensor("k", k, 4), _check_tensor("v", v, 4)
+    B, Hq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    wsb = lib.skipsm_decode_workspace_size(B, Hq, Hkv, Skv, D, num_splits)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    o = torch.empty_like(q) if out is None else out
+    counts = torch.empty(Hq, dtype=torch.int64, device=q.device)
+    opts = DecodeOpts(int(num_splits), 0.0, None, None, 0, 0)
+    res = Calibration()
+    _raise(lib.skipsm_decode_calibrate(_P(q.data_ptr()), _P(k.data_ptr()), _P(v.data_ptr()),
+                                       _P(o.data_ptr()), B, Hq, Hkv, Skv, D,
+                                       float(target_skip_ratio), int(max_iters),
+                                       _P(counts.data_ptr()), _P(ws.data_ptr()),
+                                       ws.numel() * ws.element_size(), ctypes.byref(opts),
+                                       ctypes.byref(res), _P(_stream(stream))))
+    return res.lambda_, res.skip_ratio, res.launches

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/skipsm.h"
 #include "internal.h"
@@ -214,7 +215,9 @@ int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested) {
   if (want == 0) {
     const long long items = static_cast<long long>(B) * Hkv;
     want = static_cast<int>((kDecodeTargetCtas + items - 1) / items);
-    want = std::min(want, std::max(1, nblk / 4));
+    // at least 16 tiles per split: each split's first tile is always kept (its running
+    // max starts at -inf), so short splits would cap the skip ratio
+    want = std::min(want, std::max(1, nblk / 16));
   }
   want = std::max(1, std::min(want, nblk));
   const int per = (nblk + want - 1) / want;
@@ -307,6 +310,108 @@ skipsm_status skipsm_decode(const void* q, const void* k, const void* v, void* o
                             void* workspace, size_t workspace_bytes, void* stream) {
   return skipsm_decode_ex(q, k, v, o, B, Hq, Hkv, Skv, D, lambda, skip_counts, workspace,
                           workspace_bytes, nullptr, stream);
+}
+
+// -------------------------------------------------------------- calibration
+}  // extern "C"
+
+namespace {
+
+// Bisection on log10(lambda) in [-9, 0] for the lambda whose skip ratio is closest
+// to `target`; `run(lambda, &ratio)` performs one attention call and measures it.
+template <class Run>
+skipsm_status bisect_lambda(float target, int max_iters, Run run, skipsm_calibration* res) {
+  if (!res) return fail(SKIPSM_ERR_INVALID_ARG, "result pointer is NULL");
+  if (!(target >= 0.f && target <= 1.f))
+    return fail(SKIPSM_ERR_INVALID_ARG, "target skip ratio must be in [0, 1]");
+  if (max_iters < 0 || max_iters > 64) return fail(SKIPSM_ERR_INVALID_ARG, "max_iters in [0, 64]");
+  if (max_iters == 0) max_iters = 14;
+  double lo = -9.0, hi = 0.0;
+  float best_l = 0.f, best_r = 0.f;
+  double best_d = 2.0;
+  int launches = 0;
+  for (int it = 0; it < max_iters; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    const float lam = static_cast<float>(std::pow(10.0, mid));
+    float ratio = 0.f;
+    const skipsm_status st = run(lam, &ratio);
+    ++launches;
+    if (st != SKIPSM_OK) return st;
+    const double d = std::fabs(static_cast<double>(ratio) - target);
+    if (d < best_d) { best_d = d; best_l = lam; best_r = ratio; }
+    if (ratio < target) lo = mid; else hi = mid;
+  }
+  res->lambda = best_l;
+  res->skip_ratio = best_r;
+  res->launches = launches;
+  return SKIPSM_OK;
+}
+
+skipsm_status read_counts(const uint64_t* dev, int n, std::vector<uint64_t>* host, cudaStream_t s) {
+  host->resize(n);
+  cudaError_t e = cudaMemcpyAsync(host->data(), dev, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "read skip counts");
+  return SKIPSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+skipsm_status skipsm_prefill_calibrate(const void* q, const void* k, const void* v, void* o, int B,
+                                       int Hq, int Hkv, int Sq, int Skv, int D, int causal,
+                                       float target_skip_ratio, int max_iters, uint64_t* counts,
+                                       const skipsm_prefill_opts* opts,
+                                       skipsm_calibration* result, void* stream) {
+  if (!counts) return fail(SKIPSM_ERR_INVALID_ARG, "counts scratch is NULL");
+  skipsm_prefill_opts op;
+  std::memset(&op, 0, sizeof(op));
+  if (opts) op = *opts;
+  if (op.skip_mask || op.visited_counts || op.lse)
+    return fail(SKIPSM_ERR_INVALID_ARG, "calibration takes no optional outputs");
+  op.visited_counts = counts + Hq;
+  std::vector<uint64_t> h;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto run = [&](float lam, float* ratio) -> skipsm_status {
+    skipsm_status st = skipsm_prefill_ex(q, k, v, o, B, Hq, Hkv, Sq, Skv, D, causal, lam, counts,
+                                         &op, stream);
+    if (st != SKIPSM_OK) return st;
+    if ((st = read_counts(counts, 2 * Hq, &h, s)) != SKIPSM_OK) return st;
+    uint64_t sk = 0, vis = 0;
+    for (int i = 0; i < Hq; ++i) { sk += h[i]; vis += h[Hq + i]; }
+    *ratio = vis ? static_cast<float>(static_cast<double>(sk) / static_cast<double>(vis)) : 0.f;
+    return SKIPSM_OK;
+  };
+  return bisect_lambda(target_skip_ratio, max_iters, run, result);
+}
+
+skipsm_status skipsm_decode_calibrate(const void* q, const void* k, const void* v, void* o, int B,
+                                      int Hq, int Hkv, int Skv, int D, float target_skip_ratio,
+                                      int max_iters, uint64_t* counts, void* workspace,
+                                      size_t workspace_bytes, const skipsm_decode_opts* opts,
+                                      skipsm_calibration* result, void* stream) {
+  if (!counts) return fail(SKIPSM_ERR_INVALID_ARG, "counts scratch is NULL");
+  skipsm_decode_opts op;
+  std::memset(&op, 0, sizeof(op));
+  if (opts) op = *opts;
+  if (op.skip_mask || op.lse) return fail(SKIPSM_ERR_INVALID_ARG, "calibration takes no optional outputs");
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv) return fail(SKIPSM_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  const int G = Hq / Hkv;
+  const double tiles = static_cast<double>(B) * Hkv * ((Skv + kDecodeBk - 1) / kDecodeBk);
+  std::vector<uint64_t> h;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto run = [&](float lam, float* ratio) -> skipsm_status {
+    skipsm_status st = skipsm_decode_ex(q, k, v, o, B, Hq, Hkv, Skv, D, lam, counts, workspace,
+                                        workspace_bytes, &op, stream);
+    if (st != SKIPSM_OK) return st;
+    if ((st = read_counts(counts, Hq, &h, s)) != SKIPSM_OK) return st;
+    uint64_t sk = 0;
+    for (int i = 0; i < Hq; i += G) sk += h[i];  // a group's count is repeated for its heads
+    *ratio = tiles > 0 ? static_cast<float>(static_cast<double>(sk) / tiles) : 0.f;
+    return SKIPSM_OK;
+  };
+  return bisect_lambda(target_skip_ratio, max_iters, run, result);
 }
 
 }  // extern "C"

@@ -117,8 +117,9 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
 
 /*
  * Number of KV splits a decode call uses when the caller asks for 0: enough
- * (b, kv head, split) work items to fill the GPU, each split at least 4 key
- * tiles of 64.  The key range is cut into ceil(nblk/splits)-tile splits, and
+ * (b, kv head, split) work items to fill the GPU, each split at least 16 key
+ * tiles of 64 (every split keeps its first tile, so short splits would cap the
+ * skip ratio).  The key range is cut into ceil(nblk/splits)-tile splits, and
  * empty trailing splits are dropped, so the count returned here is the
  * effective one.  Returns 0 for invalid sizes.
  */
@@ -165,6 +166,53 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
                                int B, int Hq, int Hkv, int Skv, int D, float lambda,
                                uint64_t* skip_counts, void* workspace, size_t workspace_bytes,
                                const skipsm_decode_opts* opts, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Threshold calibration                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Picking lambda for a target skip ratio ("Accelerating Long-Context Inference
+ * with Skip Softmax in NVIDIA TensorRT-LLM", "Impact on Accuracy vs. Speed": the
+ * threshold trades speed against accuracy; "NVIDIA Introduces Skip Softmax ...",
+ * "Accuracy and Sparsity Trade-offs": up to about 50% sparsity is near-lossless).
+ *
+ * The calibration runs the kernel at lambda values chosen by bisection on
+ * log10(lambda) in [1e-9, 1] and returns the evaluated lambda whose measured
+ * skip ratio is closest to `target_skip_ratio`.  The skip ratio cannot decrease
+ * when lambda grows (a tile skipped at lambda is skipped at every larger lambda),
+ * which is what makes bisection valid.  Each step synchronises `stream` to read
+ * the counts.  The outputs of the last evaluated call are left in the buffers.
+ */
+typedef struct skipsm_calibration {
+  float lambda;        /* chosen threshold */
+  float skip_ratio;    /* skipped / visited tiles measured at that threshold */
+  int launches;        /* attention calls made */
+} skipsm_calibration;
+
+/*
+ * Prefill calibration.  Arguments as skipsm_prefill_ex; `counts` is caller-owned
+ * device scratch of 2*Hq uint64 (skip counts, then visited counts).  target in
+ * [0, 1]; max_iters in [1, 64] bisection steps (0 = 14).  opts->skip_mask,
+ * opts->visited_counts and opts->lse must be NULL (opts may be NULL).
+ */
+skipsm_status skipsm_prefill_calibrate(const void* q, const void* k, const void* v, void* o,
+                                       int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                       int causal, float target_skip_ratio, int max_iters,
+                                       uint64_t* counts, const skipsm_prefill_opts* opts,
+                                       skipsm_calibration* result, void* stream);
+
+/*
+ * Decode calibration.  Arguments as skipsm_decode_ex; the skip ratio is skipped
+ * 64-key tiles over all (b, kv head) tiles.  `counts` is device scratch of Hq
+ * uint64.  opts->skip_mask and opts->lse must be NULL (opts may be NULL).
+ */
+skipsm_status skipsm_decode_calibrate(const void* q, const void* k, const void* v, void* o,
+                                      int B, int Hq, int Hkv, int Skv, int D,
+                                      float target_skip_ratio, int max_iters, uint64_t* counts,
+                                      void* workspace, size_t workspace_bytes,
+                                      const skipsm_decode_opts* opts,
+                                      skipsm_calibration* result, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Decode without a caller-provided workspace                                 */

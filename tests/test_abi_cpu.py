@@ -114,7 +114,7 @@ def test_split_geometry_matches_oracle(lib, B, Hkv, Skv, req):
     ref_req = req if req else ns
     assert oracle.decode_split_geometry(Skv, 64, ref_req)[2] == ns
     if req == 0:
-        # default: at least ~4 tiles per split, and no more splits than tiles
+        # default: no more splits than tiles
         nblk = -(-Skv // 64)
         assert ns <= max(1, nblk)
 
@@ -125,3 +125,22 @@ def test_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert bs.decode_workspace_size(8, 64, 8, 131072, 128, 0) == al(rows * 128 * 4) + al(rows * 4)
     assert bs.decode_workspace_size(8, 63, 8, 131072, 128, 0) == 0
+
+
+def test_calibration_rejects_bad_arguments(lib):
+    res = bs.Calibration()
+    cal = lib.skipsm_prefill_calibrate
+    # target outside [0, 1], bad iteration count, missing scratch or result: refused on the host
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, 1.5, 0, P, None, ctypes.byref(res), None) == 1
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, -0.1, 0, P, None, ctypes.byref(res), None) == 1
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, 0.5, 65, P, None, ctypes.byref(res), None) == 1
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, 0.5, 0, None, None, ctypes.byref(res), None) == 1
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, 0.5, 0, P, None, None, None) == 1
+    opts = bs.PrefillOpts(0, 0, 0.0, None, P, None, 0)  # a skip-mask output is not allowed
+    assert cal(P, P, P, P, 1, 2, 1, 256, 256, 128, 1, 0.5, 0, P, ctypes.byref(opts),
+               ctypes.byref(res), None) == 1
+    dcal = lib.skipsm_decode_calibrate
+    assert dcal(P, P, P, P, 1, 8, 1, 1024, 128, 2.0, 0, P, P, 1 << 20, None,
+                ctypes.byref(res), None) == 1
+    assert dcal(P, P, P, P, 1, 8, 3, 1024, 128, 0.5, 0, P, P, 1 << 20, None,
+                ctypes.byref(res), None) == 1
