@@ -16,15 +16,18 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread):
 //                 S_x = Q_x K_j^T   (A, B from shared memory, D in TMEM)
 //                 O_x += P_x V_j    (A = P from TMEM, B = V from shared memory)
-//   warp 3      idle (it only gives its registers to the softmax warps)
-//   warps 4-7   softmax of Q tile 0, warps 8-11 softmax of Q tile 1:
-//                 one thread per row = one TMEM lane; the whole S row is read
-//                 into registers at once, the row max votes, and for kept
-//                 tiles bf16 P is written over S in TMEM
-// The two Q tiles ping-pong: while one warpgroup runs its softmax the tensor
-// core works on the other tile.  The running max used by the vote is always
-// the exact prefix max; the accumulator's reference max is only moved when the
-// max has grown by more than 2^8 (lazy rescaling), which changes no result.
+//   warp 3      idle
+//   warps 4-7   softmax of both Q tiles, in the order (x=0, j), (x=1, j),
+//                 (x=0, j+1), ...: one thread per row = one TMEM lane; the whole
+//                 S row is read into registers at once, the row max votes, and
+//                 for kept tiles bf16 P is written over S in TMEM
+// While the softmax warps work on one Q tile the tensor core runs P.V and the
+// next Q.K^T of the other.  Each SMSP hosts one softmax warp: a second one would
+// take the issue slots the MMA-issuing thread needs (measured: the tensor core
+// slows by a third when two exp-heavy warps share the issuing thread's SMSP).
+// The running max used by the vote is always the exact prefix max; the
+// accumulator's reference max is only moved when the max has grown by more
+// than 2^8 (lazy rescaling), which changes no result.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmem_wide.cuh"
@@ -32,13 +35,9 @@
 namespace skipsm {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
 constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
 constexpr float kRescaleLog2 = 8.f;
-constexpr uint32_t kRegsLow = 56;   // warps 0-3 after setmaxnreg.dec
-constexpr uint32_t kRegsHigh = 216; // softmax warpgroups after setmaxnreg.inc
-// registers the launch must provide for the split above (checked on the host)
-constexpr int kRegPoolNeeded = static_cast<int>(kRegsLow * 128 + 2 * kRegsHigh * 128);
 
 template <int D, int BK, int TQ, int NK, int NV>
 struct PrefillCfg {
@@ -172,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *stmem;
 
   if (warp < 4) {
-    setmaxnreg_dec<kRegsLow>();
     if ((warp == 0 || warp == 2) && lane == 0) {
       // ============================================================ TMA
       // warp 0: Q, then the K ring; warp 2: the V ring.  The two rings advance
@@ -291,169 +289,193 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================================================ softmax
-    setmaxnreg_inc<kRegsHigh>();
-    const int x = (warp - 4) >> 2;        // Q tile
+    // One warpgroup serves both Q tiles in the order the MMA warp issues them:
+    // (x=0, j), (x=1, j), (x=0, j+1), ...  While it works on one tile, the tensor
+    // core runs P.V and the next Q.K^T of the other, and each SMSP hosts a single
+    // softmax warp, which leaves issue slots for the MMA-issuing thread.
     const int wq = warp & 3;              // TMEM lane quadrant
-    const int r = wq * 32 + lane;         // row within the Q tile
-    const int row = qrow0 + x * kQRows + r;
-    const bool valid = row < p.Sq;
+    const int r = wq * 32 + lane;         // row within a Q tile
     const int qoff = p.Skv - p.Sq;
-    const int qpos = row + qoff;
-    const int qpos_warp0 = qrow0 + x * kQRows + wq * 32 + qoff;  // smallest position in this warp
-    const int n = x == 0 ? n0 : n1;
-    const int grp = TQ == 128 ? 0 : (wq >> 1);           // vote group within the Q tile
-    const int grp_row0 = qrow0 + x * kQRows + grp * TQ;  // first row of this vote group
-    const int n_grp = tiles_visible(grp_row0, grp_row0 + TQ, p, BK);
-    const int n_half0 = tiles_visible(qrow0 + x * kQRows, qrow0 + x * kQRows + 64, p, BK);
-    const int n_half1 = tiles_visible(qrow0 + x * kQRows + 64, qrow0 + x * kQRows + 128, p, BK);
-    const int qtile = grp_row0 / TQ;
+    const int grp = TQ == 128 ? 0 : (wq >> 1);  // vote group within a Q tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
-    const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
     const float sl2 = p.scale_log2;
-    float M = -INFINITY, R = -INFINITY, l = 0.f;
+    struct TileRow {
+      int n, n_grp, n_half0, n_half1, qtile, row, qpos, qpos_warp0;
+      bool valid;
+      float M, R, l;   // running max, reference max of the accumulator, row sum
+    };
+    TileRow tr[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int t0 = qrow0 + x * kQRows;
+      const int grp_row0 = t0 + grp * TQ;
+      tr[x].n = x == 0 ? n0 : n1;
+      tr[x].n_grp = tiles_visible(grp_row0, grp_row0 + TQ, p, BK);
+      tr[x].n_half0 = tiles_visible(t0, t0 + 64, p, BK);
+      tr[x].n_half1 = tiles_visible(t0 + 64, t0 + 128, p, BK);
+      tr[x].qtile = grp_row0 / TQ;
+      tr[x].row = t0 + r;
+      tr[x].valid = tr[x].row < p.Sq;
+      tr[x].qpos = tr[x].row + qoff;
+      tr[x].qpos_warp0 = t0 + wq * 32 + qoff;  // smallest position in this warp
+      tr[x].M = -INFINITY;
+      tr[x].R = -INFINITY;
+      tr[x].l = 0.f;
+    }
     unsigned long long n_skip = 0, n_visit = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
-      tc_fence_after();
-      uint32_t sv[BK];
-      tmem_ld<BK>(tS, sv);
-      const int key0 = j * BK;
-      // tile-level (warp-uniform) test: does any row of this warp see a masked key?
-      if ((p.causal && key0 + BK - 1 > qpos_warp0) || key0 + BK > p.Skv) {
+    for (int j = 0; j < nmax; ++j) {
 #pragma unroll
-        for (int i = 0; i < BK; ++i) {
-          const int key = key0 + i;
-          const bool masked = (p.causal && key > qpos) || key >= p.Skv;
-          sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
-        }
-      }
-      // 16 independent max chains, then a tree (short dependency chains)
-      float m16[16];
+      for (int x = 0; x < 2; ++x) {
+        TileRow& t = tr[x];
+        if (j >= t.n) continue;
+        const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
+        const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
+        ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
+        tc_fence_after();
+        uint32_t sv[BK];
+        tmem_ld<BK>(tS, sv);
+        const int key0 = j * BK;
+        // tile-level (warp-uniform) test: does any row of this warp see a masked key?
+        if ((p.causal && key0 + BK - 1 > t.qpos_warp0) || key0 + BK > p.Skv) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
-#pragma unroll
-      for (int i = 16; i < BK; i += 16)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
-      const float mx = m16[0];
-      const float mt2 = valid ? mx * sl2 : -INFINITY;
-      const float d = gapf(mt2, M);
-      const bool row_vote = !valid || d < p.lam_log2;
-      const bool warp_vote = __all_sync(0xffffffffu, row_vote);
-      volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
-      if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
-      // A warp with a row that keeps the tile knows its vote group keeps it, so it
-      // only arrives on the barrier; warps whose rows all vote skip wait for every
-      // vote.  A 64-row group past its causal range never keeps the tile.  Every
-      // warp does exactly one barrier operation per tile, so the warps of a
-      // warpgroup stay matched even when a bounded wait has given up.
-      const bool out_of_range = TQ == 64 && j >= (grp == 0 ? n_half0 : n_half1);
-      bool skip_g[2];
-      if ((!warp_vote || !p.lam_pos) && !out_of_range) {
-        named_bar_arrive(1 + x, 128);
-        skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
-        skip_g[grp] = false;
-      } else {
-        named_bar_sync(1 + x, 128);
-        const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
-        if (TQ == 128) {
-          skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
-        } else {
-          // tiles past a 64-row group's causal range are not visited by it
-          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= n_half0;
-          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= n_half1;
-        }
-      }
-      const bool any_kept = !(skip_g[0] && skip_g[1]);
-      const bool my_skip = skip_g[grp];
-      if (r == grp * TQ && j < n_grp) {  // one thread per vote group records it
-        ++n_visit;
-        n_skip += my_skip ? 1 : 0;
-        if (p.skip_mask)
-          p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + qtile) * p.nkt + j] =
-              my_skip ? 1 : 0;
-      }
-      if (r == 0) sdec[x] = any_kept ? 1 : 0;
-      if (any_kept) {
-        if (!my_skip) {
-          M = fmaxf(M, mt2);
-          float alpha = 1.f;
-          bool resc = false;
-          if (M > R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
-            resc = R != -INFINITY;
-            alpha = ex2(R - M);
-            l *= alpha;
-            R = M;
+          for (int i = 0; i < BK; ++i) {
+            const int key = key0 + i;
+            const bool masked = (p.causal && key > t.qpos) || key >= p.Skv;
+            sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
           }
-          if (__any_sync(0xffffffffu, resc)) {
-            // Every earlier P.V of this Q tile is complete: the S of this tile was
-            // committed after it, and the next P.V waits for this warpgroup.
-
-            // 32 columns at a time: the S row is still live in registers
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t ov[32];
-              tmem_ld32(tO + c0, ov);
+        }
+        // 16 independent max chains, then a tree (short dependency chains)
+        float m16[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              tmem_st32(tO + c0, ov);
+        for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
+#pragma unroll
+        for (int i = 16; i < BK; i += 16)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
+        const float mx = m16[0];
+        const float mt2 = t.valid ? mx * sl2 : -INFINITY;
+        const float d = gapf(mt2, t.M);
+        const bool row_vote = !t.valid || d < p.lam_log2;
+        const bool warp_vote = __all_sync(0xffffffffu, row_vote);
+        volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
+        if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
+        // A warp with a row that keeps the tile knows its vote group keeps it, so it
+        // only arrives on the barrier; warps whose rows all vote skip wait for every
+        // vote.  A 64-row group past its causal range never keeps the tile.  Every
+        // warp does exactly one barrier operation per tile, so the warps stay
+        // matched even when a bounded wait has given up.
+        const bool out_of_range = TQ == 64 && j >= (grp == 0 ? t.n_half0 : t.n_half1);
+        bool skip_g[2];
+        if ((!warp_vote || !p.lam_pos) && !out_of_range) {
+          named_bar_arrive(1 + x, 128);
+          skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
+          skip_g[grp] = false;
+        } else {
+          named_bar_sync(1 + x, 128);
+          const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
+          if (TQ == 128) {
+            skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
+          } else {
+            // tiles past a 64-row group's causal range are not visited by it
+            skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
+            skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
+          }
+        }
+        const bool any_kept = !(skip_g[0] && skip_g[1]);
+        const bool my_skip = skip_g[grp];
+        if (r == grp * TQ && j < t.n_grp) {  // one thread per vote group records it
+          ++n_visit;
+          n_skip += my_skip ? 1 : 0;
+          if (p.skip_mask)
+            p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + t.qtile) * p.nkt + j] =
+                my_skip ? 1 : 0;
+        }
+        if (r == 0) sdec[x] = any_kept ? 1 : 0;
+        if (any_kept) {
+          if (!my_skip) {
+            t.M = fmaxf(t.M, mt2);
+            float alpha = 1.f;
+            bool resc = false;
+            if (t.M > t.R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
+              resc = t.R != -INFINITY;
+              alpha = ex2(t.R - t.M);
+              t.l *= alpha;
+              t.R = t.M;
             }
-          }
-          // P = 2^(s*scale*log2e - R) in bf16, written over S
-          const float negR = -R;
-          float la[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[BK / 2];
+            if (__any_sync(0xffffffffu, resc)) {
+              // Every earlier P.V of this Q tile is complete: the S of this tile was
+              // committed after it, and the next P.V waits for this warpgroup.
+
+              // 32 columns at a time: the S row is still live in registers
+#pragma unroll 1
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tO + c0, ov);
 #pragma unroll
-          for (int i = 0; i < BK / 2; ++i) {
-            const float e0 = ex2(fmaf(__uint_as_float(sv[2 * i]), sl2, negR));
-            const float e1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), sl2, negR));
-            la[i & 3] += e0 + e1;
-            pk[i] = pack_bf16x2(e0, e1);
-          }
-          l += (la[0] + la[1]) + (la[2] + la[3]);
-          tmem_st<BK / 2>(tS, pk);
-        } else {
-          uint32_t z[BK / 2];
+                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                tmem_st32(tO + c0, ov);
+              }
+            }
+            // P = 2^(s*scale*log2e - R) in bf16, written over S
+            const float negR = -t.R;
+            float la[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[BK / 2];
 #pragma unroll
-          for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
-          tmem_st<BK / 2>(tS, z);
+            for (int i = 0; i < BK / 2; ++i) {
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negR);
+              const float e0 = ex2(x0), e1 = ex2(x1);
+              fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
+              pk[i] = pack_bf16x2(e0, e1);
+            }
+            t.l += (la[0] + la[1]) + (la[2] + la[3]);
+            tmem_st<BK / 2>(tS, pk);
+          } else {
+            uint32_t z[BK / 2];
+#pragma unroll
+            for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
+            tmem_st<BK / 2>(tS, z);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull(x));
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      TileRow& t = tr[x];
+      if (__all_sync(0xffffffffu, ok && t.n > 0 && !*abort_flag)) {  // warp-uniform: TMEM loads below
+        // ---- epilogue: O / l -> bf16, LSE (one commit after the last P.V of this Q tile)
+        ok = mbar_wait(odone(x), 0, wc, kSitePrefillODone);
+        tc_fence_after();
+        uint32_t ov[D];
+        tmem_ld<D>(lane_base + (x == 0 ? C::kColO0 : C::kColO1), ov);
+        if (t.valid && ok) {
+          const float inv = 1.f / t.l;
+          __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row) * D;
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i)
+            dst[i] = make_uint4(
+                pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
+          if (p.lse)
+            p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row] =
+                (t.R + __log2f(t.l)) * 0.69314718055994531f;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pfull(x));
     }
-    if (__all_sync(0xffffffffu, ok && n > 0 && !*abort_flag)) {  // warp-uniform: TMEM loads below
-      // ---- epilogue: O / l -> bf16, LSE (one commit after the last P.V of this Q tile)
-      ok = mbar_wait(odone(x), 0, wc, kSitePrefillODone);
-      tc_fence_after();
-      uint32_t ov[D];
-      tmem_ld<D>(tO, ov);
-      if (valid && ok) {
-        const float inv = 1.f / l;
-        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row) * D;
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-          dst[i] = make_uint4(
-              pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
-        if (p.lse)
-          p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + row] =
-              (R + __log2f(l)) * 0.69314718055994531f;
-      }
-      if (r == grp * TQ) {
-        if (p.skip_counts && n_skip) atomicAdd(p.skip_counts + hq, n_skip);
-        if (p.visited_counts && n_visit) atomicAdd(p.visited_counts + hq, n_visit);
-      }
+    if (r == grp * TQ) {
+      if (p.skip_counts && n_skip) atomicAdd(p.skip_counts + hq, n_skip);
+      if (p.visited_counts && n_visit) atomicAdd(p.visited_counts + hq, n_visit);
     }
   }
 
@@ -472,13 +494,7 @@ cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const C
                        const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, BK, TQ, NK, NV>;
   auto kern = prefill_kernel<D, BK, TQ, NK, NV>;
-  // setmaxnreg moves registers inside the CTA's launch allocation: refuse to
-  // launch (instead of letting .inc wait forever) if that pool is too small.
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
-  if (e != cudaSuccess) return e;
-  if (attr.numRegs * kThreads < kRegPoolNeeded) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
   kern<<<grid, kThreads, C::kAlloc, stream>>>(qmap, kmap, vmap, p);
