@@ -213,40 +213,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (!mbar_try_wait(full, (j / NS) & 1) && clock64() - t0 < p.wait_cycles) {}
         }
       }
-    } else if (warp == 1 && lane == 0 && nmax > 0) {
+    } else if (warp == 1 && nmax > 0) {
       // ============================================================ MMA
+      // The whole warp runs this loop converged, so descriptors and stage indices
+      // stay warp-uniform; one elected lane issues each MMA and commit.
+      const uint32_t issue = elect_one();
       const int nx[2] = {n0, n1};
       const uint32_t colS[2] = {C::kColS0, C::kColS1};
       const uint32_t colO[2] = {C::kColO0, C::kColO1};
       bool first_pv[2] = {true, true};
+      auto wait = [&](uint32_t bar, uint32_t parity, int site) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, site));
+      };
       auto issue_s = [&](int x, int ks) {
+        const uint64_t qd = sdesc_sw128(sQ + x * C::kQTileBytes, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sK + ks * C::kKVBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qa = sQ + x * C::kQTileBytes + (kk >> 2) * (kQRows * 128) + (kk & 3) * 32;
-          const uint32_t kb = sK + ks * C::kKVBytes + (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-          umma_ss(tmem + colS[x], sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb, 16, 1024),
-                  C::kIdescQK, kk > 0 ? 1u : 0u);
+          // advance the start address (16-byte units) within / across swizzle atoms
+          const uint32_t qo = ((kk >> 2) * (kQRows * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t ko = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
+          umma_ss_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
         }
       };
       auto issue_pv = [&](int x, int vs) {
+        const uint64_t vd = sdesc_sw128(sV + vs * C::kKVBytes, BK * 128, 1024);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t vb = sV + vs * C::kKVBytes + kk * 16 * 128;
-          umma_ts(tmem + colO[x], tmem + colS[x] + kk * 8, sdesc_sw128(vb, BK * 128, 1024),
-                  C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          umma_ts_w(tmem + colO[x], tmem + colS[x] + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                    C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u, issue);
         first_pv[x] = false;
       };
-      bool ok = mbar_wait(qfull, 0, wc, kSitePrefillQ) &&
-                mbar_wait(kfull(0), 0, wc, kSitePrefillKFull);
+      bool ok = wait(qfull, 0, kSitePrefillQ) && wait(kfull(0), 0, kSitePrefillKFull);
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
           if (nx[x] > 0) {
             issue_s(x, 0);
-            umma_commit(sfull(x));
+            umma_commit_w(sfull(x), issue);
           }
-        umma_commit(kempty(0));
+        umma_commit_w(kempty(0), issue);
       }
       for (int j = 0; ok && j < nmax; ++j) {
         const int vs = j % NV, ks1 = (j + 1) % NK;
@@ -254,11 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool v_ready = false, k_ready = false;
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= nx[x]) continue;
-          if (!mbar_wait(pfull(x), j & 1, wc, kSitePrefillPFull)) { ok = false; break; }
+          if (!wait(pfull(x), j & 1, kSitePrefillPFull)) { ok = false; break; }
           tc_fence_after();
           if (sdec[x]) {
             if (!v_ready) {
-              if (!mbar_wait(vfull(vs), (j / NV) & 1, wc, kSitePrefillVFull)) { ok = false; break; }
+              if (!wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) { ok = false; break; }
               v_ready = true;
               tc_fence_after();
             }
@@ -266,24 +272,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j + 1 < nx[x]) {
             if (!k_ready) {  // K_{j+1} is first needed here, after P.V of tile j is queued
-              if (!mbar_wait(kfull(ks1), ((j + 1) / NK) & 1, wc, kSitePrefillKFull)) { ok = false; break; }
+              if (!wait(kfull(ks1), ((j + 1) / NK) & 1, kSitePrefillKFull)) { ok = false; break; }
               k_ready = true;
               tc_fence_after();
             }
             issue_s(x, ks1);
-            umma_commit(sfull(x));
+            umma_commit_w(sfull(x), issue);
           } else {
             // the last tile of this Q tile: one commit lets the epilogue wait for its final P.V
-            umma_commit(odone(x));
+            umma_commit_w(odone(x), issue);
           }
         }
         if (!ok) break;
-        if (has_next) umma_commit(kempty(ks1));
-        if (!v_ready && !mbar_wait(vfull(vs), (j / NV) & 1, wc, kSitePrefillVFull)) break;
-        umma_commit(vempty(vs));
+        if (has_next) umma_commit_w(kempty(ks1), issue);
+        if (!v_ready && !wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) break;
+        umma_commit_w(vempty(vs), issue);
       }
-      // every MMA issued by this thread completes before TMEM is released
-      umma_commit(final_bar);
+      // every MMA issued by this warp completes before TMEM is released
+      umma_commit_w(final_bar, issue);
       const long long t0 = clock64();
       while (!mbar_try_wait(final_bar, 0) && clock64() - t0 < p.wait_cycles) {}
     }
@@ -300,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = p.scale_log2;
     struct TileRow {
-      int n, n_grp, n_half0, n_half1, qtile, row, qpos, qpos_warp0;
+      int n, n_grp, n_half0, n_half1, qtile, row, qpos;
+      int j_mask;  // first key tile in which a row of this warp has a masked key
       bool valid;
       float M, R, l;   // running max, reference max of the accumulator, row sum
     };
@@ -317,13 +324,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tr[x].row = t0 + r;
       tr[x].valid = tr[x].row < p.Sq;
       tr[x].qpos = tr[x].row + qoff;
-      tr[x].qpos_warp0 = t0 + wq * 32 + qoff;  // smallest position in this warp
+      // key tile j holds a key that is masked for some row of this warp iff its
+      // last key is past the warp's smallest position (causal) or past Skv
+      const int qpos_warp0 = t0 + wq * 32 + qoff;
+      tr[x].j_mask = p.Skv / BK;
+      if (p.causal) tr[x].j_mask = min(tr[x].j_mask, (qpos_warp0 + 1) / BK);
       tr[x].M = -INFINITY;
       tr[x].R = -INFINITY;
       tr[x].l = 0.f;
     }
     unsigned long long n_skip = 0, n_visit = 0;
     bool ok = true;
+    bool next_ready = false;  // the S of the next tile in this order is known to be complete
     for (int j = 0; j < nmax; ++j) {
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
@@ -331,13 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= t.n) continue;
         const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
         const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
-        ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
+        if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
         tc_fence_after();
         uint32_t sv[BK];
         tmem_ld<BK>(tS, sv);
+        {
+          // probe the S of the next tile now; the answer is read one tile later
+          int xn = 1 - x, jn = x == 0 ? j : j + 1, nn = tr[1 - x].n;
+          if (jn >= nn) { xn = x; jn = j + 1; nn = t.n; }
+          next_ready = jn < nn && mbar_test_wait(sfull(xn), jn & 1);
+        }
         const int key0 = j * BK;
         // tile-level (warp-uniform) test: does any row of this warp see a masked key?
-        if ((p.causal && key0 + BK - 1 > t.qpos_warp0) || key0 + BK > p.Skv) {
+        if (j >= t.j_mask) {
 #pragma unroll
           for (int i = 0; i < BK; ++i) {
             const int key = key0 + i;
@@ -361,6 +379,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mt2 = t.valid ? mx * sl2 : -INFINITY;
         const float d = gapf(mt2, t.M);
         const bool row_vote = !t.valid || d < p.lam_log2;
+        bool skip_g[2];
+        if (TQ == 128) {
+          // one vote group = the whole Q tile: a barrier that ANDs the row votes
+          // (every warp does exactly one barrier operation per tile, so the warps
+          // stay matched even when a bounded wait has given up)
+          const bool sk = p.lam_pos && named_bar_and(1 + x, 128, row_vote);
+          skip_g[0] = skip_g[1] = sk;
+        } else {
         const bool warp_vote = __all_sync(0xffffffffu, row_vote);
         volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
         if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
@@ -369,8 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // vote.  A 64-row group past its causal range never keeps the tile.  Every
         // warp does exactly one barrier operation per tile, so the warps stay
         // matched even when a bounded wait has given up.
-        const bool out_of_range = TQ == 64 && j >= (grp == 0 ? t.n_half0 : t.n_half1);
-        bool skip_g[2];
+        const bool out_of_range = j >= (grp == 0 ? t.n_half0 : t.n_half1);
         if ((!warp_vote || !p.lam_pos) && !out_of_range) {
           named_bar_arrive(1 + x, 128);
           skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
@@ -378,13 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           named_bar_sync(1 + x, 128);
           const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
-          if (TQ == 128) {
-            skip_g[0] = skip_g[1] = p.lam_pos && (v0 & v1 & v2 & v3 & 1);
-          } else {
-            // tiles past a 64-row group's causal range are not visited by it
-            skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
-            skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
-          }
+          // tiles past a 64-row group's causal range are not visited by it
+          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
+          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
+        }
         }
         const bool any_kept = !(skip_g[0] && skip_g[1]);
         const bool my_skip = skip_g[grp];
