@@ -347,12 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint32_t sv[BK];
         tmem_ld<BK>(tS, sv);
-        {
-          // probe the S of the next tile now; the answer is read one tile later
-          int xn = 1 - x, jn = x == 0 ? j : j + 1, nn = tr[1 - x].n;
-          if (jn >= nn) { xn = x; jn = j + 1; nn = t.n; }
-          next_ready = jn < nn && mbar_test_wait(sfull(xn), jn & 1);
-        }
         const int key0 = j * BK;
         // tile-level (warp-uniform) test: does any row of this warp see a masked key?
         if (j >= t.j_mask) {
@@ -463,6 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
             tmem_st<BK / 2>(tS, z);
           }
+        }
+        {
+          // Probe the next tile's S without blocking; its latency overlaps the
+          // fence and arrive below, and a complete phase skips the wait.
+          int xn = 1 - x, jn = x == 0 ? j : j + 1, nn = tr[1 - x].n;
+          if (jn >= nn) { xn = x; jn = j + 1; nn = t.n; }
+          next_ready = jn < nn && mbar_test_wait(sfull(xn), jn & 1);
         }
         tc_fence_before();
         __syncwarp();
