@@ -8,7 +8,10 @@ library; the only common dependency is the seeded input generator ``synth``.
 Parity is pinned for every function here (see ``tests/test_oracle_pins.py``):
 dense attention from a library routine at lambda = 0, an independent
 closed-form skip mask, a closed-form output over the kept keys, monotonicity
-in lambda, the analytic error bound, and hand-derived worked examples.
+in lambda, the analytic error bound, and hand-derived worked examples.  The
+optional Rowmax-PoT weights are pinned in ``tests/test_oracle_pot.py`` (worked
+examples, reduction to dense softmax for integer exponents, a bound against
+dense softmax, planted mistakes).
 """
 
 from .skipsm_oracle import (  # noqa: F401

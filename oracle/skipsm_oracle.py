@@ -39,6 +39,23 @@ Readings where the pages are silent
   running max at -inf and the split results are merged by an exact
   log-sum-exp combine.
 
+Rowmax-PoT weights (optional, prefill)
+--------------------------------------
+"Approximating Softmax in Pretrained LLMs: Model Sensitivity and Kernel
+Acceleration", AI Summary and Abstract: exponentials are replaced by powers of
+two, a coarse logarithmic weight representation anchored at each row maximum.
+Reading used here (the pages give no formula): for a kept tile, with m'_r the
+row maximum after the tile (the same exact running maximum the skip rule uses),
+key c gets the weight 2^n, n = round((s_rc - m'_r) * log2 e) (ties to even),
+and 0 when that exponent is below -126.5 (the smallest normal fp32 power of
+two is 2^-126).  Earlier tiles are rescaled exactly by exp(m_r - m'_r) when
+the maximum grows, as in the exact recurrence, so each key's weight is anchored
+at the running maximum of the tile it belongs to.  The pages' "Rowmax-H15"
+hardware specialisation is not described and is not modelled.  Because the
+rounding of n decides a discrete value, keys whose exponent lies within
+POT_AMBIGUOUS_BAND of a rounding boundary are reported: a kernel computing the
+logits in fp32 may round them the other way.
+
 Everything is fp64; bf16 inputs convert to fp64 exactly.  There is no blocking,
 fusion or reordering beyond the tile loop that defines the method.
 """
@@ -52,6 +69,10 @@ from typing import List, Optional, Tuple
 import numpy as np
 
 NEG_INF = -np.inf
+LOG2E = 1.0 / math.log(2.0)
+# half-width (in log2 units) of the band around a rounding boundary of the
+# Rowmax-PoT exponent inside which an fp32 computation may round differently
+POT_AMBIGUOUS_BAND = 1e-4
 
 
 # ---------------------------------------------------------------------------
@@ -102,6 +123,33 @@ def _online_update(m: np.ndarray, l: np.ndarray, o: np.ndarray, s: np.ndarray,
     return m_new, l_new, o_new
 
 
+def _pot_weights(s: np.ndarray, m_new: np.ndarray):
+    """Rowmax-PoT weights of one tile: (w, ambiguous) with w_rc = 2^round((s - m')*log2 e),
+    0 below 2^-126.5, and ambiguous_rc true where the exponent is within
+    POT_AMBIGUOUS_BAND of a rounding boundary."""
+    with np.errstate(invalid="ignore"):
+        x = (s - m_new[:, None]) * LOG2E              # <= 0; -inf for masked keys
+    x = np.maximum(x, -127.0)
+    n = np.rint(x)                                    # ties to even
+    w = np.where(n < -126.0, 0.0, np.exp2(n))
+    amb = (np.abs(x - (np.floor(x) + 0.5)) < POT_AMBIGUOUS_BAND) & (x > -127.0)
+    return w, amb
+
+
+def _online_update_pot(m: np.ndarray, l: np.ndarray, o: np.ndarray, a: np.ndarray,
+                       s: np.ndarray, vtile: np.ndarray):
+    """The online update with Rowmax-PoT weights; `a` is the running weight of
+    ambiguous keys, in the units of l."""
+    m_new = np.maximum(m, np.max(s, axis=1))
+    with np.errstate(invalid="ignore"):
+        alpha = np.where(m == NEG_INF, 0.0, np.exp(m - m_new))
+    w, amb = _pot_weights(s, m_new)
+    l_new = alpha * l + w.sum(axis=1)
+    o_new = alpha[:, None] * o + w @ vtile
+    a_new = alpha * a + (w * amb).sum(axis=1)
+    return m_new, l_new, o_new, a_new
+
+
 def _finish(m: np.ndarray, l: np.ndarray, o: np.ndarray):
     return o / l[:, None], m + np.log(l)
 
@@ -115,6 +163,9 @@ class PrefillResult:
     lse: np.ndarray     # [B][Hq][Sq] natural log
     mask: np.ndarray    # int8 [B][Hq][nqt][nkt]: -1 not visited, 0 kept, 1 skipped
     margin: np.ndarray  # fp64, same shape; +inf where the decision cannot flip
+    # Rowmax-PoT only: per row, the fraction of the weight sum carried by keys whose
+    # exponent rounding is ambiguous in fp32 (None for exact exponentials)
+    pot_ambiguous: Optional[np.ndarray] = None
 
     @property
     def skip_counts(self) -> np.ndarray:
@@ -132,10 +183,12 @@ def last_visible_key(r1: int, Sq: int, Skv: int, causal: bool) -> int:
 
 
 def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, tile_q: int,
-                  tile_k: int, causal: bool, lam: float, scale: float):
-    """One query tile of one head: returns (o_rows, lse_rows, mask[nkt], margin[nkt]).
+                  tile_k: int, causal: bool, lam: float, scale: float, pot: bool = False):
+    """One query tile of one head: returns (o_rows, lse_rows, mask[nkt], margin[nkt],
+    ambiguous_fraction_rows or None).
 
-    qh is the head's full query matrix [Sq][D]; kh, vh its kv head [Skv][D].
+    qh is the head's full query matrix [Sq][D]; kh, vh its kv head [Skv][D].  With
+    pot=True kept tiles take Rowmax-PoT weights instead of exact exponentials.
     """
     Sq, Skv = qh.shape[0], kh.shape[0]
     nkt = (Skv + tile_k - 1) // tile_k
@@ -146,6 +199,7 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
     m = np.full(n, NEG_INF)
     l = np.zeros(n)
     o = np.zeros((n, qh.shape[1]))
+    a = np.zeros(n)
     mask = np.full(nkt, -1, dtype=np.int8)
     margin = np.full(nkt, np.inf)
     last_tile = last_visible_key(r1, Sq, Skv, causal) // tile_k
@@ -158,14 +212,20 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
         margin[j] = mg
         if skip:
             continue
-        m, l, o = _online_update(m, l, o, s, vh[c0:c1])
+        if pot:
+            m, l, o, a = _online_update_pot(m, l, o, a, s, vh[c0:c1])
+        else:
+            m, l, o = _online_update(m, l, o, s, vh[c0:c1])
+    amb = a / l if pot else None
     o, lse = _finish(m, l, o)
-    return o, lse, mask, margin
+    return o, lse, mask, margin, amb
 
 
 def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: float,
-            tile_q: int, tile_k: int, scale: Optional[float] = None) -> PrefillResult:
-    """Skip Softmax prefill over q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] (fp64)."""
+            tile_q: int, tile_k: int, scale: Optional[float] = None,
+            pot: bool = False) -> PrefillResult:
+    """Skip Softmax prefill over q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] (fp64); pot=True
+    uses Rowmax-PoT weights on kept tiles."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     if Hq % Hkv or (causal and Sq > Skv):
@@ -178,16 +238,20 @@ def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: f
     lse = np.zeros((B, Hq, Sq))
     mask = np.full((B, Hq, nqt, nkt), -1, dtype=np.int8)
     margin = np.full((B, Hq, nqt, nkt), np.inf)
+    amb = np.zeros((B, Hq, Sq)) if pot else None
     for b in range(B):
         for h in range(Hq):
             kh, vh = k[b, h // G], v[b, h // G]
             for t in range(nqt):
                 r0, r1 = t * tile_q, min((t + 1) * tile_q, Sq)
-                ot, lt, mt, gt = prefill_qtile(q[b, h], kh, vh, t, tile_q=tile_q, tile_k=tile_k,
-                                               causal=causal, lam=lam, scale=scale)
+                ot, lt, mt, gt, at = prefill_qtile(q[b, h], kh, vh, t, tile_q=tile_q,
+                                                   tile_k=tile_k, causal=causal, lam=lam,
+                                                   scale=scale, pot=pot)
                 o[b, h, r0:r1], lse[b, h, r0:r1] = ot, lt
                 mask[b, h, t], margin[b, h, t] = mt, gt
-    return PrefillResult(o, lse, mask, margin)
+                if pot:
+                    amb[b, h, r0:r1] = at
+    return PrefillResult(o, lse, mask, margin, amb)
 
 
 # ---------------------------------------------------------------------------

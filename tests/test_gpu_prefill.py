@@ -25,9 +25,9 @@ def _compare_heads(w, q, k, v, out, lam, heads, qtiles=None):
         nqt = -(-w.Sq // out.tile_q)
         for t in (range(nqt) if qtiles is None else qtiles):
             r0, r1 = t * out.tile_q, min((t + 1) * out.tile_q, w.Sq)
-            ot, lt, mt, gt = oracle.prefill_qtile(qh, kh, vh, t, tile_q=out.tile_q,
-                                                  tile_k=out.tile_k, causal=w.causal, lam=lam,
-                                                  scale=1.0 / np.sqrt(w.D))
+            ot, lt, mt, gt, _ = oracle.prefill_qtile(qh, kh, vh, t, tile_q=out.tile_q,
+                                                     tile_k=out.tile_k, causal=w.causal, lam=lam,
+                                                     scale=1.0 / np.sqrt(w.D))
             assert_close(to_f64(o[b, h, r0:r1]), ot, f"o[b={b},h={h},t={t}]")
             assert np.all(np.abs(lse[b, h, r0:r1] - lt) < 2e-2), f"lse[b={b},h={h},t={t}]"
             low += assert_masks(mask[b, h, t], mt, gt, f"mask[b={b},h={h},t={t}]")
