@@ -395,6 +395,20 @@ def run_ours(args):
             "executed_tflops": prefill_exec_flops(wp, visited, sk, 128, 128) / sec / 1e12,
             "speedup_vs_lambda0": t_dense / sec, "max_abs_err_vs_lambda0": err_max,
             "mean_abs_err_vs_lambda0": err_mean})
+    # Rowmax-PoT weights on the kept tiles (same skip decisions), against the exact lambda=0 output
+    sweep_pot = []
+    for lam in (0.0, lam_pf[TARGET_RHO]):
+        def run_pot():
+            bs.prefill(q, k, v, lam, causal=True, out=o, skip_counts=cnt, exp_mode="pot")
+        sec = time_events(run_pot, 3)
+        d = (o.float() - o_ref.float()).abs()
+        sk = int(cnt.sum().item())
+        sweep_pot.append({
+            "lambda": lam, "skip_ratio": sk / visited, "ms": sec * 1e3,
+            "dense_equiv_tflops": prefill_dense_flops(wp) / sec / 1e12,
+            "speedup_vs_exact_lambda0": t_dense / sec,
+            "max_abs_err_vs_exact_lambda0": float(d.max()),
+            "mean_abs_err_vs_exact_lambda0": float(d.mean())})
     del o_ref
     od_ref = None
     sweep_dec = []
@@ -523,7 +537,7 @@ def run_ours(args):
                    "hbm_gbs_on_bytes_read": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9,
                    "hbm_frac_of_measured": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9
                    / peaks["hbm_gbs"], "skip_ratio": rho_dec, "lambda": lam_dec},
-        "sweep": {"prefill": sweep_pf, "decode": sweep_dec},
+        "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "roofline": roofline,

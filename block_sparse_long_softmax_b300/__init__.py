@@ -36,7 +36,16 @@ class PrefillOpts(ctypes.Structure):
     _fields_ = [("tile_q", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("softmax_scale", ctypes.c_float), ("lse", ctypes.c_void_p),
                 ("skip_mask", ctypes.c_void_p), ("visited_counts", ctypes.c_void_p),
-                ("wait_limit_ms", ctypes.c_int)]
+                ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int)]
+
+
+EXP_MODES = {"exact": 0, "pot": 1}
+
+
+def _exp_mode(exp_mode) -> int:
+    if exp_mode not in EXP_MODES:
+        raise ValueError(f"exp_mode must be one of {sorted(EXP_MODES)}")
+    return EXP_MODES[exp_mode]
 
 
 class DecodeOpts(ctypes.Structure):
@@ -136,8 +145,11 @@ class PrefillOut:
 def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k: int = 0,
             softmax_scale: float = 0.0, return_lse: bool = False, return_mask: bool = False,
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
-            wait_limit_ms: int = 0) -> PrefillOut:
-    """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors."""
+            wait_limit_ms: int = 0, exp_mode: str = "exact") -> PrefillOut:
+    """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors.
+
+    exp_mode "exact" uses exponentials on kept tiles, "pot" Rowmax-PoT powers of two.
+    """
     import torch
     lib = library()
     _check_tensor("q", q, 4), _check_tensor("k", k, 4), _check_tensor("v", v, 4)
@@ -153,7 +165,7 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     vis = torch.empty(Hq, dtype=torch.int64, device=q.device) if return_visited else None
     ptr = lambda t: _P(t.data_ptr()) if t is not None else _P(0)  # noqa: E731
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
-                       ptr(vis).value, int(wait_limit_ms))
+                       ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode))
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))
@@ -205,7 +217,8 @@ def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0
 
 
 def calibrate_prefill(q, k, v, target_skip_ratio: float, causal: bool = True, *, tile_q: int = 0,
-                      tile_k: int = 0, max_iters: int = 0, out=None, stream=None):
+                      tile_k: int = 0, max_iters: int = 0, out=None, stream=None,
+                      exp_mode: str = "exact"):
     """lambda whose measured prefill tile skip ratio is closest to the target.
 
     Returns (lambda, skip_ratio, launches).  Runs the kernel max_iters times (default 14).
@@ -217,7 +230,7 @@ def calibrate_prefill(q, k, v, target_skip_ratio: float, causal: bool = True, *,
     Hkv, Skv = k.shape[1], k.shape[2]
     o = torch.empty_like(q) if out is None else out
     counts = torch.empty(2 * Hq, dtype=torch.int64, device=q.device)
-    opts = PrefillOpts(tile_q, tile_k, 0.0, None, None, None, 0)
+    opts = PrefillOpts(tile_q, tile_k, 0.0, None, None, None, 0, _exp_mode(exp_mode))
     res = Calibration()
     _raise(lib.skipsm_prefill_calibrate(_P(q.data_ptr()), _P(k.data_ptr()), _P(v.data_ptr()),
                                         _P(o.data_ptr()), B, Hq, Hkv, Sq, Skv, D,

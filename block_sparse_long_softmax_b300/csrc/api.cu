@@ -158,6 +158,8 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
     return fail(SKIPSM_ERR_UNSUPPORTED, "tile_q / tile_k must be 64 or 128");
   if (!(op.softmax_scale >= 0.f) || !std::isfinite(op.softmax_scale))
     return fail(SKIPSM_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  if (op.exp_mode != 0 && op.exp_mode != 1)
+    return fail(SKIPSM_ERR_INVALID_ARG, "exp_mode must be 0 (exact) or 1 (Rowmax-PoT)");
   const long long nblk_q = (Sq + 255) / 256;
   if (nblk_q * B * Hq > 0x7FFFFFFFLL) return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
   int* status = device_status_word();
@@ -186,6 +188,7 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.skip_mask = op.skip_mask;
   p.status = status;
   p.wait_cycles = wait_cycles(op.wait_limit_ms);
+  p.exp_mode = op.exp_mode;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

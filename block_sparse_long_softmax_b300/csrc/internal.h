@@ -67,6 +67,7 @@ struct PrefillParams {
   float scale_log2;
   float lam_log2;
   int lam_pos;
+  int exp_mode;          // 0 exact exponentials, 1 Rowmax-PoT weights
   __nv_bfloat16* o;      // [B][Hq][Sq][D]
   float* lse;            // [B][Hq][Sq] or null
   unsigned long long* skip_counts;

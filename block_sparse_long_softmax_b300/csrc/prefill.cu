@@ -98,13 +98,8 @@ template <>
 __device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
 template <>
 __device__ __forceinline__ void tmem_st<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
-template <>
-__device__ __forceinline__ void tmem_st<128>(uint32_t taddr, const uint32_t (&r)[128]) {
-  tmem_st64(taddr, *reinterpret_cast<const uint32_t(*)[64]>(&r[0]));
-  tmem_st64(taddr + 64, *reinterpret_cast<const uint32_t(*)[64]>(&r[64]));
-}
 
-template <int D, int BK, int TQ, int NK, int NV>
+template <int D, int BK, int TQ, int NK, int NV, bool POT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
@@ -437,17 +432,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32(tO + c0, ov);
               }
             }
-            // P = 2^(s*scale*log2e - R) in bf16, written over S
-            const float negR = -t.R;
             float la[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[BK / 2];
+            if constexpr (!POT) {
+              // P = 2^(s*scale*log2e - R) in bf16, written over S
+              const float negR = -t.R;
 #pragma unroll
-            for (int i = 0; i < BK / 2; ++i) {
-              float x0, x1;
-              ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negR);
-              const float e0 = ex2(x0), e1 = ex2(x1);
-              fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
-              pk[i] = pack_bf16x2(e0, e1);
+              for (int i = 0; i < BK / 2; ++i) {
+                float x0, x1;
+                ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negR);
+                const float e0 = ex2(x0), e1 = ex2(x1);
+                fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
+                pk[i] = pack_bf16x2(e0, e1);
+              }
+            } else {
+              // Rowmax-PoT ("Approximating Softmax in Pretrained LLMs ...", Abstract):
+              // the weight is 2^n, n = round(s*scale*log2e - M), anchored at the running
+              // row max M, and 0 below 2^-126.5.  n is rounded (ties to even) by adding
+              // 1.5*2^23, whose fp32 bits are then 0x4B400000 + n; shifting those bits
+              // by 23 and adding the bits of 1.0 builds the fp32 bits of 2^n (n = -127
+              // gives 0).  The factor 2^(M - R) to the accumulator's reference R is
+              // rounded to bf16, so P = 2^n * c is exact in bf16 and the row sum adds
+              // exactly what the MMA multiplies.
+              const float negM = -t.M;
+              const float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
+#pragma unroll
+              for (int i = 0; i < BK / 2; ++i) {
+                float x0, x1;
+                ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negM);
+                x0 = fmaxf(x0, -127.f);
+                x1 = fmaxf(x1, -127.f);
+                float y0, y1;
+                ffma2(y0, y1, x0, x1, 1.f, 12582912.f);
+                const float p0 = __uint_as_float(__float_as_uint(y0) * 8388608u + 0x3F800000u);
+                const float p1 = __uint_as_float(__float_as_uint(y1) * 8388608u + 0x3F800000u);
+                float e0, e1;
+                ffma2(e0, e1, p0, p1, c, 0.f);
+                fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
+                pk[i] = pack_bf16x2(e0, e1);
+              }
             }
             t.l += (la[0] + la[1]) + (la[2] + la[3]);
             tmem_st<BK / 2>(tS, pk);
@@ -512,11 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK, int TQ, int NK, int NV>
+template <int D, int BK, int TQ, int NK, int NV, bool POT>
 cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, BK, TQ, NK, NV>;
-  auto kern = prefill_kernel<D, BK, TQ, NK, NV>;
+  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
@@ -528,9 +551,10 @@ cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const C
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillParams& p, cudaStream_t stream) {
-#define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)        \
-  if (p.D == d && p.tile_k == bk && p.tile_q == tq) \
-    return launch_cfg<d, bk, tq, nk, nv>(qmap, kmap, vmap, p, stream);
+#define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)                                     \
+  if (p.D == d && p.tile_k == bk && p.tile_q == tq)                              \
+    return p.exp_mode == 1 ? launch_cfg<d, bk, tq, nk, nv, true>(qmap, kmap, vmap, p, stream) \
+                           : launch_cfg<d, bk, tq, nk, nv, false>(qmap, kmap, vmap, p, stream);
   SKIPSM_PREFILL_CASE(128, 128, 128, 3, 2)
   SKIPSM_PREFILL_CASE(128, 128, 64, 3, 2)
   SKIPSM_PREFILL_CASE(128, 64, 128, 4, 4)

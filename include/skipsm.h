@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 100
+#define SKIPSM_VERSION 101
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -87,6 +87,14 @@ typedef struct skipsm_prefill_opts {
                              0 kept, 1 skipped, 2 not visited (causal) — fully written */
   uint64_t* visited_counts; /* optional out [Hq]: visited tile pairs per head (zeroed, filled) */
   int wait_limit_ms;      /* bound of each pipeline wait in the kernel; 0 = 2000 ms */
+  int exp_mode;           /* weights of the kept tiles' keys:
+                             0 = exact exponentials exp(s - m');
+                             1 = Rowmax-PoT ("Approximating Softmax in Pretrained LLMs: Model
+                                 Sensitivity and Kernel Acceleration", AI Summary, Abstract):
+                                 2^round((s - m') * log2 e), anchored at the running row max m'
+                                 after the key's tile, 0 below 2^-126.5 (the skip vote is
+                                 unchanged: it always uses the exact maxima);
+                             other values: SKIPSM_ERR_INVALID_ARG */
 } skipsm_prefill_opts;
 
 /*

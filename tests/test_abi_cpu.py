@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.skipsm_version() == 100
+    assert lib.skipsm_version() == 101
 
 
 P = 0x10000  # a 16-byte aligned fake device address; validation never dereferences it
@@ -80,6 +80,18 @@ def test_prefill_rejects_tiles(lib, tq, tk):
 
 def test_prefill_rejects_bad_scale(lib):
     assert _prefill(lib, opts=bs.PrefillOpts(0, 0, -1.0, None, None, None, 0)) == 1
+
+
+@pytest.mark.parametrize("mode", [-1, 2, 7])
+def test_prefill_rejects_bad_exp_mode(lib, mode):
+    assert _prefill(lib, opts=bs.PrefillOpts(0, 0, 0.0, None, None, None, 0, mode)) == 1
+    assert "exp_mode" in lib.skipsm_last_error().decode()
+
+
+def test_binding_rejects_unknown_exp_mode():
+    with pytest.raises(ValueError):
+        bs._exp_mode("poly")
+    assert bs._exp_mode("exact") == 0 and bs._exp_mode("pot") == 1
 
 
 @pytest.mark.parametrize("kw,status", [
