@@ -447,23 +447,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else {
               // Rowmax-PoT ("Approximating Softmax in Pretrained LLMs ...", Abstract):
-              // the weight is 2^n, n = round(s*scale*log2e - M), anchored at the running
-              // row max M, and 0 below 2^-126.5.  n is rounded (ties to even) by adding
-              // 1.5*2^23, whose fp32 bits are then 0x4B400000 + n; shifting those bits
-              // by 23 and adding the bits of 1.0 builds the fp32 bits of 2^n (n = -127
-              // gives 0).  The factor 2^(M - R) to the accumulator's reference R is
-              // rounded to bf16, so P = 2^n * c is exact in bf16 and the row sum adds
-              // exactly what the MMA multiplies.
-              const float negM = -t.M;
+              // the weight is 2^n, n = round(x), x = s*scale*log2e - M, anchored at the
+              // running row max M, and 0 below 2^-126.5.  One saturating FMA gives
+              // u = clamp(1 + x/127, 0, 1) (masked keys, -inf, give 0); adding
+              // 1.5*2^23 - 127 to 127*u rounds x to n (ties to even) and leaves the fp32
+              // bits 0x4B400000 + n; shifting those bits by 23 and adding the bits of
+              // 1.0 builds the fp32 bits of 2^n (n = -127 gives 0).  The factor
+              // 2^(M - R) to the accumulator's reference R is rounded to bf16, so
+              // P = 2^n * c is exact in bf16 and the row sum adds exactly what the MMA
+              // multiplies.  The fp32 error of x is below 3e-5, well inside the band
+              // in which the exponent's rounding is treated as ambiguous.
+              const float ua = sl2 * (1.f / 127.f);
+              const float ub = 1.f - t.M * (1.f / 127.f);
               const float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
 #pragma unroll
               for (int i = 0; i < BK / 2; ++i) {
-                float x0, x1;
-                ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negM);
-                x0 = fmaxf(x0, -127.f);
-                x1 = fmaxf(x1, -127.f);
+                const float u0 = sat_fma(__uint_as_float(sv[2 * i]), ua, ub);
+                const float u1 = sat_fma(__uint_as_float(sv[2 * i + 1]), ua, ub);
                 float y0, y1;
-                ffma2(y0, y1, x0, x1, 1.f, 12582912.f);
+                ffma2(y0, y1, u0, u1, 127.f, 12582912.f - 127.f);
                 const float p0 = __uint_as_float(__float_as_uint(y0) * 8388608u + 0x3F800000u);
                 const float p1 = __uint_as_float(__float_as_uint(y1) * 8388608u + 0x3F800000u);
                 float e0, e1;

@@ -28,6 +28,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// a * b + c clamped to [0, 1] (NaN -> 0), one FMA
+__device__ __forceinline__ float sat_fma(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // (d0, d1) = (a0, a1) * b + c, as one packed fp32x2 FMA
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
