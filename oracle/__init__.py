@@ -11,7 +11,9 @@ closed-form skip mask, a closed-form output over the kept keys, monotonicity
 in lambda, the analytic error bound, and hand-derived worked examples.  The
 optional Rowmax-PoT weights are pinned in ``tests/test_oracle_pot.py`` (worked
 examples, reduction to dense softmax for integer exponents, a bound against
-dense softmax, planted mistakes).
+dense softmax, planted mistakes); the optional decode block mask in
+``tests/test_oracle_blockmask.py`` (SDPA over the selected keys, invariance to
+unselected keys, worked examples, planted mistakes).
 """
 
 from .skipsm_oracle import (  # noqa: F401

@@ -39,6 +39,17 @@ Readings where the pages are silent
   running max at -inf and the split results are merged by an exact
   log-sum-exp combine.
 
+Caller-supplied block mask (optional, decode)
+---------------------------------------------
+"NVIDIA Introduces Skip Softmax ...", "Benefits and Implementation": Skip Softmax
+can be combined with other sparse-attention methods.  Reading used here: a
+block selector hands the decode a mask over the 64-key tiles of each (batch,
+kv head); tiles outside it are not visited at all (no logits, no running max,
+no vote), and the skip rule runs over the selected tiles of each split in
+ascending order, the first selected tile of a split being always kept.  A split
+with no selected tile contributes nothing to the combine; a group with no
+selected tile at all gets output 0 and log-sum-exp -inf.
+
 Rowmax-PoT weights (optional, prefill)
 --------------------------------------
 "Approximating Softmax in Pretrained LLMs: Model Sensitivity and Kernel
@@ -261,7 +272,7 @@ def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: f
 class DecodeResult:
     o: np.ndarray       # [B][Hq][D]
     lse: np.ndarray     # [B][Hq]
-    mask: np.ndarray    # int8 [B][Hkv][nblk]: 0 kept, 1 skipped
+    mask: np.ndarray    # int8 [B][Hkv][nblk]: 0 kept, 1 skipped, -1 not selected
     margin: np.ndarray  # [B][Hkv][nblk]
     num_splits: int     # splits actually used (after dropping empty ones)
 
@@ -281,9 +292,11 @@ def decode_split_geometry(Skv: int, tile_k: int, num_splits: int) -> Tuple[int, 
 
 
 def decode_group(qg: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, lam: float,
-                 num_splits: int, tile_k: int = 64, scale: Optional[float] = None):
+                 num_splits: int, tile_k: int = 64, scale: Optional[float] = None,
+                 block_mask: Optional[np.ndarray] = None):
     """One GQA group: qg [G][D] against kv head kh, vh [Skv][D].
 
+    block_mask, if given, is a boolean [nblk] of the key tiles to visit.
     Returns (o [G][D], lse [G], mask [nblk], margin [nblk], per-split (o, lse) list).
     """
     G, D = qg.shape
@@ -298,6 +311,9 @@ def decode_group(qg: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, lam: float,
         l = np.zeros(G)
         o = np.zeros((G, D))
         for j in range(sp * per, min((sp + 1) * per, nblk)):
+            if block_mask is not None and not block_mask[j]:
+                mask[j] = -1
+                continue
             c0, c1 = j * tile_k, min((j + 1) * tile_k, Skv)
             s = _tile_logits(qg, kh[c0:c1], scale, np.zeros(G), np.arange(c0, c1), False)
             d = _row_gap(np.max(s, axis=1), m)
@@ -307,10 +323,15 @@ def decode_group(qg: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, lam: float,
             if skip:
                 continue
             m, l, o = _online_update(m, l, o, s, vh[c0:c1])
-        parts.append(_finish(m, l, o))
-    # exact log-sum-exp combine of the split results
+        if np.all(l == 0.0):       # no selected tile in this split
+            parts.append((np.zeros((G, D)), np.full(G, NEG_INF)))
+        else:
+            parts.append(_finish(m, l, o))
+    # exact log-sum-exp combine of the split results (empty splits weigh 0)
     lses = np.stack([p[1] for p in parts])          # [nsplit][G]
     top = lses.max(axis=0)
+    if np.all(top == NEG_INF):
+        return np.zeros((G, D)), np.full(G, NEG_INF), mask, margin, parts
     wts = np.exp(lses - top[None, :])
     o = sum(wts[i][:, None] * parts[i][0] for i in range(nsplit)) / wts.sum(axis=0)[:, None]
     lse = top + np.log(wts.sum(axis=0))
@@ -318,8 +339,10 @@ def decode_group(qg: np.ndarray, kh: np.ndarray, vh: np.ndarray, *, lam: float,
 
 
 def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, lam: float, num_splits: int,
-           tile_k: int = 64, scale: Optional[float] = None) -> DecodeResult:
-    """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] (fp64)."""
+           tile_k: int = 64, scale: Optional[float] = None,
+           block_mask: Optional[np.ndarray] = None) -> DecodeResult:
+    """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] (fp64); block_mask, if given,
+    is a boolean [B][Hkv][nblk] of the key tiles each group visits."""
     B, Hq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     if Hq % Hkv:
@@ -334,7 +357,9 @@ def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, lam: float, num_split
         for hk in range(Hkv):
             og, lg, mg, gg, _ = decode_group(q[b, hk * G:(hk + 1) * G], k[b, hk], v[b, hk],
                                              lam=lam, num_splits=num_splits, tile_k=tile_k,
-                                             scale=scale)
+                                             scale=scale,
+                                             block_mask=None if block_mask is None
+                                             else block_mask[b, hk])
             o[b, hk * G:(hk + 1) * G], lse[b, hk * G:(hk + 1) * G] = og, lg
             mask[b, hk], margin[b, hk] = mg, gg
     return DecodeResult(o, lse, mask, margin, nsplit)
