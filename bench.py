@@ -113,9 +113,11 @@ def prefill_exec_flops(w, visited: int, skipped: int, tq: int, tk: int) -> float
     return per * visited + per * (visited - skipped)
 
 
-def decode_bytes(w, kept_tiles: int, nsplit: int) -> float:
-    """Bytes a decode step must move: all K, V of kept tiles, q, o, split partials."""
-    k = w.B * w.Hkv * w.Skv * w.D * 2
+def decode_bytes(w, kept_tiles: int, nsplit: int, visited_tiles=None) -> float:
+    """Bytes a decode step must move: K of the visited tiles (all of them without a block
+    mask), V of kept tiles, q, o, split partials."""
+    k = (w.B * w.Hkv * w.Skv * w.D * 2 if visited_tiles is None
+         else visited_tiles * 64 * w.D * 2)
     v = kept_tiles * 64 * w.D * 2
     qo = 2 * w.B * w.Hq * w.D * 2
     ws = 2 * w.B * w.Hq * nsplit * (w.D + 1) * 4
@@ -429,6 +431,28 @@ def run_ours(args):
             "speedup_vs_lambda0": t_dense_d / sec, "model_speedup_2_over_2_minus_rho": 2 / (2 - rho),
             "max_abs_err_vs_lambda0": e_max})
 
+    # Skip Softmax behind a block selector: a seeded mask keeps the first and the last
+    # 64 tiles of every group (sink and recent window) and half of the others at random
+    nb = -(-wd.Skv // 64)
+    gsel = torch.Generator(device="cpu").manual_seed(1234 + rank)
+    selm = torch.rand((wd.B, wd.Hkv, nb), generator=gsel) < 0.5
+    selm[:, :, :64] = True
+    selm[:, :, -64:] = True
+    selm = selm.to(torch.uint8).to(dev)
+    n_sel = int(selm.sum().item())
+    sweep_bm = []
+    for lam in [0.0, lam_dec]:
+        def run_bm():
+            bs.decode(qd, kd, vd, lam, workspace=wsp, out=od, skip_counts=cntd, block_mask=selm)
+        sec = time_events(run_bm, 20)
+        skipped = int(cntd[:: wd.G].sum().item())
+        sweep_bm.append({
+            "lambda": lam, "selected_fraction": n_sel / nblk_d,
+            "skip_ratio_of_selected": skipped / n_sel, "us": sec * 1e6,
+            "hbm_gbs_on_bytes_read": decode_bytes(wd, n_sel - skipped, nsplit, n_sel) / sec / 1e9,
+            "speedup_vs_unmasked_lambda0": t_dense_d / sec})
+    del selm
+
     # ---- the timed steps
     lam_step = lam_pf[TARGET_RHO]
     ev_pf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -537,7 +561,8 @@ def run_ours(args):
                    "hbm_gbs_on_bytes_read": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9,
                    "hbm_frac_of_measured": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9
                    / peaks["hbm_gbs"], "skip_ratio": rho_dec, "lambda": lam_dec},
-        "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot},
+        "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot,
+                  "decode_block_mask": sweep_bm},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "roofline": roofline,

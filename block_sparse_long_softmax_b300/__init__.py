@@ -51,7 +51,8 @@ def _exp_mode(exp_mode) -> int:
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("lse", ctypes.c_void_p), ("skip_mask", ctypes.c_void_p),
-                ("wait_limit_ms", ctypes.c_int), ("inject_wait_timeout", ctypes.c_int)]
+                ("wait_limit_ms", ctypes.c_int), ("inject_wait_timeout", ctypes.c_int),
+                ("block_mask", ctypes.c_void_p)]
 
 
 class Calibration(ctypes.Structure):
@@ -192,8 +193,12 @@ class DecodeOut:
 def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0.0,
            return_lse: bool = False, return_mask: bool = False, workspace=None, out=None,
            skip_counts=None, stream=None, wait_limit_ms: int = 0,
-           inject_wait_timeout: bool = False) -> DecodeOut:
-    """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors."""
+           inject_wait_timeout: bool = False, block_mask=None) -> DecodeOut:
+    """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors.
+
+    block_mask: optional uint8/bool CUDA tensor [B][Hkv][ceil(Skv/64)] of the key tiles
+    to visit (nonzero = visit).
+    """
     import torch
     lib = library()
     _check_tensor("q", q, 3), _check_tensor("k", k, 4), _check_tensor("v", v, 4)
@@ -208,8 +213,14 @@ def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0
     nblk = -(-Skv // 64)
     mask = torch.empty((B, Hkv, nblk), dtype=torch.uint8, device=q.device) if return_mask else None
     ptr = lambda t: _P(t.data_ptr()) if t is not None else _P(0)  # noqa: E731
+    if block_mask is not None:
+        if (not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda
+                or block_mask.dtype not in (torch.uint8, torch.bool)
+                or tuple(block_mask.shape) != (B, Hkv, nblk) or not block_mask.is_contiguous()):
+            raise TypeError(f"block_mask must be a contiguous uint8/bool CUDA tensor "
+                            f"of shape {(B, Hkv, nblk)}")
     opts = DecodeOpts(int(num_splits), float(softmax_scale), ptr(lse).value, ptr(mask).value,
-                      int(wait_limit_ms), 1 if inject_wait_timeout else 0)
+                      int(wait_limit_ms), 1 if inject_wait_timeout else 0, ptr(block_mask).value)
     _raise(lib.skipsm_decode_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Skv, D, float(lam),
                                 ptr(cnt), ptr(ws), ws.numel() * ws.element_size(),
                                 ctypes.byref(opts), _P(_stream(stream))))

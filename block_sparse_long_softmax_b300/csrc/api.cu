@@ -292,11 +292,25 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
   p.status = status;
   p.wait_cycles = wait_cycles(op.wait_limit_ms);
   p.inject_fault = op.inject_wait_timeout ? 1 : 0;
+  p.block_mask = op.block_mask;
+  cudaError_t e;
+  if (p.block_mask) {
+    int dev = 0, optin = 0;
+    if ((e = cudaGetDevice(&dev)) ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+      return cuda_fail(e, "query shared memory limit");
+    if (decode_smem_bytes(p) > static_cast<size_t>(optin))
+      return fail(SKIPSM_ERR_UNSUPPORTED,
+                  "block mask: a split of %d tiles does not fit in shared memory; use more splits",
+                  p.per);
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
   if (skip_counts && (e = cudaMemsetAsync(skip_counts, 0, sizeof(uint64_t) * Hq, s)))
     return cuda_fail(e, "zero skip_counts");
+  if (p.block_mask && op.skip_mask &&
+      (e = cudaMemsetAsync(op.skip_mask, 2, static_cast<size_t>(B) * Hkv * nblk, s)))
+    return cuda_fail(e, "initialise skip_mask");
   if ((e = launch_decode(kmap, vmap, p, B, s))) return cuda_fail(e, "decode split launch");
   CombineParams c;
   c.ws_o = p.ws_o;

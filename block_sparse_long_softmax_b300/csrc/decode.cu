@@ -15,6 +15,12 @@
 // so the V load of a kept tile overlaps LAG tiles of key streaming.  The
 // split result (O / l, log2 LSE) goes to the workspace; a second kernel merges
 // the splits with an exact log-sum-exp combine.
+//
+// With a caller-supplied block mask ("NVIDIA Introduces Skip Softmax ...",
+// "Benefits and Implementation": Skip Softmax combined with a block selector)
+// the CTA first compacts the selected tiles of its split into a list in shared
+// memory; every role then walks that list instead of the whole split, so an
+// unselected tile is never read.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -45,6 +51,8 @@ struct DecodeCfg {
   static constexpr int kOffAbort = kOffBar + kNBar * 8;
   static constexpr int kBytes = kOffAbort + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  // block-mask tile list: [count int, pad to 16][uint16 tile offsets within the split]
+  static constexpr int kOffSel = (kBytes + 15) & ~15;
   static_assert(4 * D * 8 * 4 <= NK * kStageBytes, "final reduction buffer aliases K stages");
   static_assert(NK <= kNDec, "decision ring must cover the key prefetch depth");
 };
@@ -95,7 +103,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     *abort_flag = 0;
     mbar_fence_init();
   }
+  int* snsel = reinterpret_cast<int*>(smem + C::kOffSel);
+  uint16_t* sel = reinterpret_cast<uint16_t*>(smem + C::kOffSel + 16);
+  if (p.block_mask && warp == 0) {
+    // compact the selected tiles of this split (ascending) with ballots
+    const uint8_t* mrow = p.block_mask + (static_cast<size_t>(b) * p.Hkv + hkv) * p.nblk + j0;
+    int cnt = 0;
+    for (int base = 0; base < nb; base += 32) {
+      const int i = base + lane;
+      const bool on = i < nb && mrow[i] != 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, on);
+      if (on) sel[cnt + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(i);
+      cnt += __popc(bal);
+    }
+    if (lane == 0) *snsel = cnt;
+  }
   __syncthreads();
+  // tiles this CTA visits, and the split-relative index of the i-th of them
+  const int nvis = p.block_mask ? *snsel : nb;
+  auto tile_of = [&](int i) { return p.block_mask ? static_cast<int>(sel[i]) : i; };
 
   // ------------------------------------------------------------ producer --
   if (warp == 4) {
@@ -114,24 +140,24 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * 8192, map, bar, h * 64, tile * kBk, zc);
     };
-    for (int s = 0; s < NK && s < nb; ++s) {
-      load_tile(&kmap, kst + s * C::kStageBytes, kfull(s), j0 + s);
+    for (int s = 0; s < NK && s < nvis; ++s) {
+      load_tile(&kmap, kst + s * C::kStageBytes, kfull(s), j0 + tile_of(s));
       k_issued[s] = 1;
     }
     int nv = 0;
-    for (int i = 0; i < nb; ++i) {
+    for (int i = 0; i < nvis; ++i) {
       if (!mbar_wait(decbar(i % kNDec), (i / kNDec) & 1, wc, kSiteDecodeDec)) break;
       if (sdec[i % kNDec]) {
         const int vs = nv % NV;
         if (nv >= NV && !mbar_wait(vempty(vs), ((nv / NV) - 1) & 1, wc, kSiteDecodeVEmpty)) break;
-        load_tile(&vmap, vst + vs * C::kStageBytes, vfull(vs), j0 + i);
+        load_tile(&vmap, vst + vs * C::kStageBytes, vfull(vs), j0 + tile_of(i));
         ++v_issued[vs];
         ++nv;
       }
-      if (i + NK < nb) {
+      if (i + NK < nvis) {
         const int ks = i % NK;
         if (!mbar_wait(kempty(ks), (i / NK) & 1, wc, kSiteDecodeKEmpty)) break;
-        load_tile(&kmap, kst + ks * C::kStageBytes, kfull(ks), j0 + i + NK);
+        load_tile(&kmap, kst + ks * C::kStageBytes, kfull(ks), j0 + tile_of(i + NK));
         ++k_issued[ks];
       }
     }
@@ -187,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float sl2 = p.scale_log2;
   uint8_t* slot_base = smem + C::kOffSlot;
 
-  for (int i = 0; i < nb + LAG; ++i) {
-    if (i < nb) {
+  for (int i = 0; i < nvis + LAG; ++i) {
+    if (i < nvis) {
       // ---- S-phase of tile i
       const int st = i % NK;
       mbar_wait(kfull(st), (i / NK) & 1, wc, kSiteDecodeKFull);
@@ -205,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(kempty(st));
-      const int key0 = (j0 + i) * kBk + 16 * warp + g;
+      const int jt = j0 + tile_of(i);  // key tile index
+      const int key0 = jt * kBk + 16 * warp + g;
       const float s0 = key0 < p.Skv ? acc[0] * sl2 : -INFINITY;
       const float s1 = key0 < p.Skv ? acc[1] * sl2 : -INFINITY;
       const float s2 = key0 + 8 < p.Skv ? acc[2] * sl2 : -INFINITY;
@@ -233,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         sdec[i % kNDec] = skip ? 0 : 1;
         mbar_arrive(decbar(i % kNDec));
         if (p.skip_mask)
-          p.skip_mask[(static_cast<size_t>(b) * p.Hkv + hkv) * p.nblk + j0 + i] = skip ? 1 : 0;
+          p.skip_mask[(static_cast<size_t>(b) * p.Hkv + hkv) * p.nblk + jt] = skip ? 1 : 0;
       }
       n_skip += skip ? 1 : 0;
       kept_hist = (kept_hist << 1) | (skip ? 0u : 1u);
@@ -308,12 +335,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float sum = ored[(0 * D + d) * 8 + h] + ored[(1 * D + d) * 8 + h] +
                       ored[(2 * D + d) * 8 + h] + ored[(3 * D + d) * 8 + h];
     const float l = lred[h] + lred[8 + h] + lred[16 + h] + lred[24 + h];
-    p.ws_o[((row0 + h) * p.nsplit + split) * D + d] = sum / l;
+    p.ws_o[((row0 + h) * p.nsplit + split) * D + d] = l > 0.f ? sum / l : 0.f;
   }
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
     const float l = lred[h] + lred[8 + h] + lred[16 + h] + lred[24 + h];
-    p.ws_lse[(row0 + h) * p.nsplit + split] = rred[h] + __log2f(l);
+    // a split with no visited tile (block mask) weighs nothing in the combine
+    p.ws_lse[(row0 + h) * p.nsplit + split] = l > 0.f ? rred[h] + __log2f(l) : -INFINITY;
   }
   if (threadIdx.x == 0 && p.skip_counts && n_skip) {
     for (int h = 0; h < G; ++h)
@@ -327,6 +355,12 @@ __global__ void decode_combine_kernel(const CombineParams p) {
   const float* lse = p.ws_lse + static_cast<size_t>(row) * p.nsplit;
   float top = -INFINITY;
   for (int s = 0; s < p.nsplit; ++s) top = fmaxf(top, lse[s]);
+  if (top == -INFINITY) {  // no visited key at all (block mask): output 0, LSE -inf
+    for (int d = threadIdx.x; d < p.D; d += blockDim.x)
+      p.o[static_cast<size_t>(row) * p.D + d] = __float2bfloat16_rn(0.f);
+    if (p.lse && threadIdx.x == 0) p.lse[row] = -INFINITY;
+    return;
+  }
   float wsum = 0.f;
   for (int s = 0; s < p.nsplit; ++s) wsum += ex2(lse[s] - top);
   for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
@@ -339,18 +373,31 @@ __global__ void decode_combine_kernel(const CombineParams p) {
 }
 
 template <int D, int NK, int NV, int LAG>
+size_t split_smem(const DecodeParams& p) {
+  using C = DecodeCfg<D, NK, NV, LAG>;
+  // the list region starts at most 15 bytes past kBytes: pad by 16
+  return p.block_mask ? C::kAlloc + 16 + ((2 * static_cast<size_t>(p.per) + 15) & ~size_t(15)) + 16
+                      : C::kAlloc;
+}
+
+template <int D, int NK, int NV, int LAG>
 cudaError_t launch_split(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                          int B, cudaStream_t stream) {
-  using C = DecodeCfg<D, NK, NV, LAG>;
   auto kern = decode_split_kernel<D, NK, NV, LAG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+  const size_t smem = split_smem<D, NK, NV, LAG>(p);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(p.nsplit, p.Hkv, B);
-  kern<<<grid, kThreads, C::kAlloc, stream>>>(kmap, vmap, p);
+  kern<<<grid, kThreads, smem, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t decode_smem_bytes(const DecodeParams& p) {
+  return p.D == 128 ? split_smem<128, 4, 2, 1>(p) : split_smem<64, 6, 3, 1>(p);
+}
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           int B, cudaStream_t stream) {

@@ -44,6 +44,7 @@ struct DecodeParams {
   int* status;
   long long wait_cycles;
   int inject_fault;  // test hook: wait on a barrier nothing arrives at
+  const uint8_t* block_mask;  // [B][Hkv][nblk] tiles to visit, or null for all
 };
 
 struct CombineParams {
@@ -56,6 +57,8 @@ struct CombineParams {
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const DecodeParams& p, int B, cudaStream_t stream);
+// shared memory of one split CTA (with the block-mask tile list when p.block_mask is set)
+size_t decode_smem_bytes(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, int B, cudaStream_t stream);
 
 struct PrefillParams {

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 101
+#define SKIPSM_VERSION 102
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -145,11 +145,22 @@ typedef struct skipsm_decode_opts {
   int num_splits;         /* 0 = skipsm_decode_num_splits(B, Hkv, Skv, 0) */
   float softmax_scale;    /* 0 = 1/sqrt(D) */
   float* lse;             /* optional out [B][Hq] fp32 natural-log LSE */
-  uint8_t* skip_mask;     /* optional out [B][Hkv][ceil(Skv/64)]: 0 kept, 1 skipped */
+  uint8_t* skip_mask;     /* optional out [B][Hkv][ceil(Skv/64)]: 0 kept, 1 skipped
+                             (2 not selected, with block_mask) */
   int wait_limit_ms;      /* bound of each pipeline wait; 0 = 2000 ms */
   int inject_wait_timeout; /* failure-detection test hook: one split-kernel wait is made to
                               run out (nothing arrives on its barrier); the kernels end early,
                               outputs are undefined and skipsm_check() reports site 7 */
+  const uint8_t* block_mask; /* optional in, device [B][Hkv][ceil(Skv/64)]: nonzero = visit
+                              the 64-key tile.  Skip Softmax combined with a block selector
+                              ("NVIDIA Introduces Skip Softmax ...", "Benefits and
+                              Implementation"): tiles outside the mask are neither read nor
+                              voted on and do not enter the running max; the skip rule runs over
+                              the selected tiles of each split in ascending order; skip_mask
+                              reports them as 2; a group with no selected tile gets o = 0 and
+                              lse = -inf.  NULL = every tile.  With a mask each split's tile
+                              list is kept in shared memory (2 bytes per tile of the split);
+                              SKIPSM_ERR_UNSUPPORTED if it does not fit. */
 } skipsm_decode_opts;
 
 /*
