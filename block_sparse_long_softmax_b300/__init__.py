@@ -36,7 +36,8 @@ class PrefillOpts(ctypes.Structure):
     _fields_ = [("tile_q", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("softmax_scale", ctypes.c_float), ("lse", ctypes.c_void_p),
                 ("skip_mask", ctypes.c_void_p), ("visited_counts", ctypes.c_void_p),
-                ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int)]
+                ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int),
+                ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
@@ -115,12 +116,13 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _check_tensor(name, t, ndim):
+def _check_tensor(name, t, ndim, fp8=False):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype != torch.bfloat16 or t.dim() != ndim or not t.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous bf16 tensor with {ndim} dims")
+    want = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    if t.dtype != want or t.dim() != ndim or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {want} tensor with {ndim} dims")
 
 
 def check(stream=None) -> int:
@@ -146,19 +148,23 @@ class PrefillOut:
 def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k: int = 0,
             softmax_scale: float = 0.0, return_lse: bool = False, return_mask: bool = False,
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
-            wait_limit_ms: int = 0, exp_mode: str = "exact") -> PrefillOut:
-    """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors.
+            wait_limit_ms: int = 0, exp_mode: str = "exact",
+            qk_descale: float = 0.0) -> PrefillOut:
+    """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
-    exp_mode "exact" uses exponentials on kept tiles, "pot" Rowmax-PoT powers of two.
+    q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
+    Q.K^T in e4m3, scaled by qk_descale); v is bf16.  exp_mode "exact" uses exponentials on
+    kept tiles, "pot" Rowmax-PoT powers of two.
     """
     import torch
     lib = library()
-    _check_tensor("q", q, 4), _check_tensor("k", k, 4), _check_tensor("v", v, 4)
+    fp8 = q.dtype == torch.float8_e4m3fn
+    _check_tensor("q", q, 4, fp8), _check_tensor("k", k, 4, fp8), _check_tensor("v", v, 4)
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     tq = tile_q or (64 if D == 64 else 128)
     tk = tile_k or (64 if D == 64 else 128)
-    o = torch.empty_like(q) if out is None else out
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
     cnt = torch.empty(Hq, dtype=torch.int64, device=q.device) if skip_counts is None else skip_counts
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if return_lse else None
     nqt, nkt = -(-Sq // tq), -(-Skv // tk)
@@ -166,7 +172,8 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     vis = torch.empty(Hq, dtype=torch.int64, device=q.device) if return_visited else None
     ptr = lambda t: _P(t.data_ptr()) if t is not None else _P(0)  # noqa: E731
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
-                       ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode))
+                       ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
+                       float(qk_descale))
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))

@@ -54,16 +54,19 @@ EncodeTiledFn encode_fn() {
 
 // bf16 tensor [Z][S][D] (D innermost) seen as 3-D with a (64 x rows x 1) box
 // and 128-byte swizzle; out-of-range elements read as zero.
+// 3-D map (D, S, Z) of a [Z][S][D] tensor of bf16 (elem = 2) or 8-bit (elem = 1) values;
+// the box is one 128-byte swizzle row of D by box_rows rows.
 skipsm_status make_map(CUtensorMap* m, const void* base, int D, long long S, long long Z,
-                       int box_rows) {
+                       int box_rows, int elem = 2) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(SKIPSM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(Z)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem, static_cast<cuuint64_t>(S) * D * elem};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                   3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SKIPSM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -160,14 +163,21 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
     return fail(SKIPSM_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
   if (op.exp_mode != 0 && op.exp_mode != 1)
     return fail(SKIPSM_ERR_INVALID_ARG, "exp_mode must be 0 (exact) or 1 (Rowmax-PoT)");
+  if (op.qk_format != 0 && op.qk_format != 1)
+    return fail(SKIPSM_ERR_INVALID_ARG, "qk_format must be 0 (bf16) or 1 (e4m3)");
+  if (op.qk_format == 1 && (D != 128 || tk != 128))
+    return fail(SKIPSM_ERR_UNSUPPORTED, "e4m3 q/k need D = 128 and tile_k = 128");
+  if (!(op.qk_descale >= 0.f) || !std::isfinite(op.qk_descale))
+    return fail(SKIPSM_ERR_INVALID_ARG, "qk_descale must be finite and >= 0");
   const long long nblk_q = (Sq + 255) / 256;
   if (nblk_q * B * Hq > 0x7FFFFFFFLL) return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
   int* status = device_status_word();
   if (!status) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
 
   CUtensorMap qmap, kmap, vmap;
-  if ((st = make_map(&qmap, q, D, Sq, static_cast<long long>(B) * Hq, 128))) return st;
-  if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, tk))) return st;
+  const int qk_elem = op.qk_format == 1 ? 1 : 2;
+  if ((st = make_map(&qmap, q, D, Sq, static_cast<long long>(B) * Hq, 128, qk_elem))) return st;
+  if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, tk, qk_elem))) return st;
   if ((st = make_map(&vmap, v, D, Skv, static_cast<long long>(B) * Hkv, tk))) return st;
 
   PrefillParams p;
@@ -178,9 +188,11 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.nqt = (Sq + tq - 1) / tq;
   p.nkt = (Skv + tk - 1) / tk;
   p.nblk_q = static_cast<int>(nblk_q);
-  const double scale = op.softmax_scale > 0.f ? op.softmax_scale : 1.0 / std::sqrt((double)D);
+  const double scale = (op.softmax_scale > 0.f ? op.softmax_scale : 1.0 / std::sqrt((double)D)) *
+                       (op.qk_descale > 0.f ? op.qk_descale : 1.0);
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   set_lambda(lambda, &p.lam_log2, &p.lam_pos);
+  p.qk_e4m3 = op.qk_format == 1 ? 1 : 0;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = op.lse;
   p.skip_counts = reinterpret_cast<unsigned long long*>(skip_counts);

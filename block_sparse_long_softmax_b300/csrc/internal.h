@@ -71,6 +71,7 @@ struct PrefillParams {
   float lam_log2;
   int lam_pos;
   int exp_mode;          // 0 exact exponentials, 1 Rowmax-PoT weights
+  int qk_e4m3;           // Q and K are e4m3 (V stays bf16)
   __nv_bfloat16* o;      // [B][Hq][Sq][D]
   float* lse;            // [B][Hq][Sq] or null
   unsigned long long* skip_counts;

@@ -39,14 +39,20 @@ constexpr int kThreads = 256;
 constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
 constexpr float kRescaleLog2 = 8.f;
 
-template <int D, int BK, int TQ, int NK, int NV>
+template <int D, int BK, int TQ, int NK, int NV, bool F8>
 struct PrefillCfg {
-  static constexpr int kQTileBytes = kQRows * D * 2;
-  static constexpr int kKVBytes = BK * D * 2;
+  // Q and K are bf16, or e4m3 with F8; V is always bf16.  Operand rows are cut into
+  // 128-byte swizzle atoms along D: kAtoms of them, kAtomElems elements each.
+  static constexpr int kQKElem = F8 ? 1 : 2;
+  static constexpr int kAtoms = D * kQKElem / 128;
+  static constexpr int kAtomElems = 128 / kQKElem;
+  static constexpr int kQTileBytes = kQRows * D * kQKElem;
+  static constexpr int kKBytes = BK * D * kQKElem;
+  static constexpr int kVBytes = BK * D * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
-  static constexpr int kOffV = kOffK + NK * kKVBytes;
-  static constexpr int kOffBar = kOffV + NV * kKVBytes;
+  static constexpr int kOffV = kOffK + NK * kKBytes;
+  static constexpr int kOffBar = kOffV + NV * kVBytes;
   // barriers: qfull, kfull[NK], kempty[NK], vfull[NV], vempty[NV], sfull[2],
   //           pfull[2], odone[2], final
   static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 1;
@@ -60,9 +66,10 @@ struct PrefillCfg {
   static constexpr int kColS0 = 0, kColS1 = BK, kColO0 = 2 * BK, kColO1 = 2 * BK + D;
   static constexpr int kTmemUsed = 2 * BK + 2 * D;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256u : 512u;
-  static constexpr uint32_t kIdescQK = idesc_bf16(kQRows, BK, false, false);
+  static constexpr uint32_t kIdescQK = F8 ? idesc_e4m3(kQRows, BK) : idesc_bf16(kQRows, BK, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kQRows, D, false, true);
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!F8 || D == 128, "e4m3 Q/K: one 128-byte atom per row needs D = 128");
   static_assert(BK == 64 || BK == 128, "key tile");
   static_assert(TQ == 64 || TQ == 128, "vote rows");
   static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -99,12 +106,12 @@ __device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[
 template <>
 __device__ __forceinline__ void tmem_st<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT>
+template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using C = PrefillCfg<D, BK, TQ, NK, NV>;
+  using C = PrefillCfg<D, BK, TQ, NK, NV, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -181,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int zq = b * p.Hq + hq;
         mbar_arrive_expect_tx(qfull, 2 * C::kQTileBytes);
         for (int x = 0; x < 2; ++x)
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull, h * 64,
-                        qrow0 + x * kQRows, zq);
+          for (int h = 0; h < C::kAtoms; ++h)
+            tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull,
+                        h * C::kAtomElems, qrow0 + x * kQRows, zq);
       }
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
@@ -193,9 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= NS && !mbar_wait(empty, ((j / NS) - 1) & 1, wc,
                                   is_k ? kSitePrefillKEmpty : kSitePrefillVEmpty))
           break;
-        mbar_arrive_expect_tx(full, C::kKVBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(ring + st * C::kKVBytes + h * BK * 128, map, full, h * 64, j * BK, zk);
+        const int bytes = is_k ? C::kKBytes : C::kVBytes;
+        const int atoms = is_k ? C::kAtoms : D / 64;
+        const int atom_elems = is_k ? C::kAtomElems : 64;
+        mbar_arrive_expect_tx(full, bytes);
+        for (int h = 0; h < atoms; ++h)
+          tma_load_3d(ring + st * bytes + h * BK * 128, map, full, h * atom_elems, j * BK, zk);
         ++issued;
       }
       if (*abort_flag) {
@@ -222,17 +232,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_s = [&](int x, int ks) {
         const uint64_t qd = sdesc_sw128(sQ + x * C::kQTileBytes, 16, 1024);
-        const uint64_t kd = sdesc_sw128(sK + ks * C::kKVBytes, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sK + ks * C::kKBytes, 16, 1024);
+        // each MMA covers 32 bytes of the reduction (16 bf16 or 32 e4m3 elements)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D * C::kQKElem / 32; ++kk) {
           // advance the start address (16-byte units) within / across swizzle atoms
           const uint32_t qo = ((kk >> 2) * (kQRows * 128) + (kk & 3) * 32) >> 4;
           const uint32_t ko = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-          umma_ss_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
+          if constexpr (F8)
+            umma_ss_f8_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
+          else
+            umma_ss_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
         }
       };
       auto issue_pv = [&](int x, int vs) {
-        const uint64_t vd = sdesc_sw128(sV + vs * C::kKVBytes, BK * 128, 1024);
+        const uint64_t vd = sdesc_sw128(sV + vs * C::kVBytes, BK * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           umma_ts_w(tmem + colO[x], tmem + colS[x] + kk * 8, vd + ((kk * 16 * 128) >> 4),
@@ -537,11 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT>
+template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8>
 cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const PrefillParams& p, cudaStream_t stream) {
-  using C = PrefillCfg<D, BK, TQ, NK, NV>;
-  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT>;
+  using C = PrefillCfg<D, BK, TQ, NK, NV, F8>;
+  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
@@ -554,9 +568,17 @@ cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const C
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillParams& p, cudaStream_t stream) {
 #define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)                                     \
-  if (p.D == d && p.tile_k == bk && p.tile_q == tq)                              \
-    return p.exp_mode == 1 ? launch_cfg<d, bk, tq, nk, nv, true>(qmap, kmap, vmap, p, stream) \
-                           : launch_cfg<d, bk, tq, nk, nv, false>(qmap, kmap, vmap, p, stream);
+  if (p.D == d && p.tile_k == bk && p.tile_q == tq && !p.qk_e4m3)                \
+    return p.exp_mode == 1 ? launch_cfg<d, bk, tq, nk, nv, true, false>(qmap, kmap, vmap, p, stream) \
+                           : launch_cfg<d, bk, tq, nk, nv, false, false>(qmap, kmap, vmap, p, stream);
+  // e4m3 Q and K: 128-row vote groups or 64, 128-key tiles, D = 128
+  if (p.qk_e4m3 && p.D == 128 && p.tile_k == 128) {
+    if (p.tile_q == 128)
+      return p.exp_mode == 1 ? launch_cfg<128, 128, 128, 4, 3, true, true>(qmap, kmap, vmap, p, stream)
+                             : launch_cfg<128, 128, 128, 4, 3, false, true>(qmap, kmap, vmap, p, stream);
+    return p.exp_mode == 1 ? launch_cfg<128, 128, 64, 4, 3, true, true>(qmap, kmap, vmap, p, stream)
+                           : launch_cfg<128, 128, 64, 4, 3, false, true>(qmap, kmap, vmap, p, stream);
+  }
   SKIPSM_PREFILL_CASE(128, 128, 128, 3, 2)
   SKIPSM_PREFILL_CASE(128, 128, 64, 3, 2)
   SKIPSM_PREFILL_CASE(128, 64, 128, 4, 4)

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 102
+#define SKIPSM_VERSION 103
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -95,6 +95,13 @@ typedef struct skipsm_prefill_opts {
                                  after the key's tile, 0 below 2^-126.5 (the skip vote is
                                  unchanged: it always uses the exact maxima);
                              other values: SKIPSM_ERR_INVALID_ARG */
+  int qk_format;          /* element type of q and k: 0 = bf16; 1 = e4m3 (OCP FP8, 1 byte,
+                             same [B][H][S][D] layouts, D = 128 and tile_k = 128 only) for the
+                             FP8/BF16 mixed-precision path ("Approximating Softmax in Pretrained
+                             LLMs: ...", AI Summary): Q.K^T runs as an e4m3 tcgen05 MMA with
+                             fp32 accumulation, v, P and o stay bf16 */
+  float qk_descale;       /* multiplies Q.K^T before the softmax scale (the product of the q and
+                             k quantisation scales); 0 = 1 */
 } skipsm_prefill_opts;
 
 /*

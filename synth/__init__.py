@@ -17,6 +17,7 @@ from .planted import (  # noqa: F401
     bf16_bits_to_f64,
     bf16_bits_to_f32,
     f32_to_bf16_bits,
+    e4m3_round,
     normal_bits,
     WORKLOADS,
 )

@@ -163,6 +163,24 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
 
 
+def e4m3_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest OCP FP8 E4M3 value (ties to even), as fp64.
+
+    E4M3: 4 exponent bits with bias 7, 3 mantissa bits, no infinities; normal values
+    from 2^-6 to 448, subnormals in steps of 2^-9.  Magnitudes above 448 saturate
+    to 448 (the inputs generated here stay far below it).  Used only to prepare
+    FP8 test inputs; every step is exact in fp64.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                     # a = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex.astype(np.float64) - 1.0, -6.0)  # subnormals share the 2^-9 spacing
+    step = np.exp2(e - 3.0)
+    q = np.rint(a / step) * step
+    q = np.minimum(q, 448.0)
+    return np.copysign(q, x)
+
+
 # --------------------------------------------------------------------------
 # planted tables
 # --------------------------------------------------------------------------

@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.skipsm_version() == 102
+    assert lib.skipsm_version() == 103
 
 
 P = 0x10000  # a 16-byte aligned fake device address; validation never dereferences it
@@ -86,6 +86,15 @@ def test_prefill_rejects_bad_scale(lib):
 def test_prefill_rejects_bad_exp_mode(lib, mode):
     assert _prefill(lib, opts=bs.PrefillOpts(0, 0, 0.0, None, None, None, 0, mode)) == 1
     assert "exp_mode" in lib.skipsm_last_error().decode()
+
+
+@pytest.mark.parametrize("fmt,tk,D,descale,status", [
+    (2, 0, 128, 0.0, 1), (-1, 0, 128, 0.0, 1), (1, 64, 128, 0.0, 2), (1, 0, 64, 0.0, 2),
+    (0, 0, 128, -1.0, 1), (1, 0, 128, float("nan"), 1),
+])
+def test_prefill_rejects_bad_qk_format(lib, fmt, tk, D, descale, status):
+    opts = bs.PrefillOpts(0, tk, 0.0, None, None, None, 0, 0, fmt, descale)
+    assert _prefill(lib, D=D, opts=opts) == status
 
 
 def test_binding_rejects_unknown_exp_mode():

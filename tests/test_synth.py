@@ -71,3 +71,20 @@ def test_prefill_window_bump():
     planted_far = P.key_planted(w, t, 0, 0, 0, w.Skv)[(i - 3 * w.window).clip(min=0)]
     assert recent.mean() > 6.0
     assert abs(far[~planted_far].mean()) < 1.0
+
+
+def test_e4m3_round_matches_worked_values_and_torch():
+    # worked values of OCP E4M3 (3 mantissa bits, bias 7): ties go to the even mantissa
+    # (-7.75 lies halfway between 7.5 and 8 and goes to 8, mantissa 000)
+    x = np.array([1.0, 1.0625, 1.1875, 448.0, 500.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10,
+                  -7.75, 0.0, 2.0 ** -6 * 1.0625])
+    want = np.array([1.0, 1.0, 1.25, 448.0, 448.0, 2.0 ** -9, 0.0, 2.0 ** -8, -8.0, 0.0,
+                     2.0 ** -6])
+    assert np.array_equal(synth.e4m3_round(x), want)
+    # and torch's own cast (float8_e4m3fn) on bf16-representable values
+    rng = np.random.default_rng(0)
+    v = synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(
+        (rng.standard_normal(50000) * 8).astype(np.float32)))
+    import torch
+    t = torch.tensor(v).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(synth.e4m3_round(v), t)
