@@ -411,6 +411,23 @@ def run_ours(args):
             "speedup_vs_exact_lambda0": t_dense / sec,
             "max_abs_err_vs_exact_lambda0": float(d.max()),
             "mean_abs_err_vs_exact_lambda0": float(d.mean())})
+    # FP8/BF16 mixed precision: e4m3 Q and K (the same inputs rounded), bf16 V
+    q8, k8 = q.to(torch.float8_e4m3fn), k.to(torch.float8_e4m3fn)
+    sweep_fp8 = []
+    for lam in (0.0, lam_pf[TARGET_RHO]):
+        def run_fp8():
+            bs.prefill(q8, k8, v, lam, causal=True, out=o, skip_counts=cnt)
+        sec = time_events(run_fp8, 3)
+        d = (o.float() - o_ref.float()).abs()
+        sk = int(cnt.sum().item())
+        sweep_fp8.append({
+            "lambda": lam, "skip_ratio": sk / visited, "ms": sec * 1e3,
+            "dense_equiv_tflops": prefill_dense_flops(wp) / sec / 1e12,
+            "executed_tflops": prefill_exec_flops(wp, visited, sk, 128, 128) / sec / 1e12,
+            "speedup_vs_bf16_lambda0": t_dense / sec,
+            "max_abs_err_vs_bf16_lambda0": float(d.max()),
+            "mean_abs_err_vs_bf16_lambda0": float(d.mean())})
+    del q8, k8
     del o_ref
     od_ref = None
     sweep_dec = []
@@ -562,7 +579,7 @@ def run_ours(args):
                    "hbm_frac_of_measured": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9
                    / peaks["hbm_gbs"], "skip_ratio": rho_dec, "lambda": lam_dec},
         "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot,
-                  "decode_block_mask": sweep_bm},
+                  "decode_block_mask": sweep_bm, "prefill_fp8_qk": sweep_fp8},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "roofline": roofline,
