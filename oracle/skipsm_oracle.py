@@ -39,16 +39,18 @@ Readings where the pages are silent
   running max at -inf and the split results are merged by an exact
   log-sum-exp combine.
 
-Caller-supplied block mask (optional, decode)
----------------------------------------------
+Caller-supplied block mask (optional, prefill and decode)
+--------------------------------------------------------
 "NVIDIA Introduces Skip Softmax ...", "Benefits and Implementation": Skip Softmax
-can be combined with other sparse-attention methods.  Reading used here: a
-block selector hands the decode a mask over the 64-key tiles of each (batch,
-kv head); tiles outside it are not visited at all (no logits, no running max,
-no vote), and the skip rule runs over the selected tiles of each split in
-ascending order, the first selected tile of a split being always kept.  A split
-with no selected tile contributes nothing to the combine; a group with no
-selected tile at all gets output 0 and log-sum-exp -inf.
+can be combined with other sparse-attention methods (a block selector in
+prefill).  Reading used here: a block selector hands the kernel a mask over the
+(query tile, key tile) pairs of prefill, or over the 64-key tiles of each
+(batch, kv head) in decode; tiles outside it are not visited at all (no
+logits, no running max, no vote), and the skip rule runs over the selected
+tiles in ascending order, the first selected tile being always kept (in decode:
+the first of each split).  A decode split with no selected tile contributes
+nothing to the combine; a row (prefill) or group (decode) that ends with no
+visible selected key gets output 0 and log-sum-exp -inf.
 
 Rowmax-PoT weights (optional, prefill)
 --------------------------------------
@@ -194,12 +196,14 @@ def last_visible_key(r1: int, Sq: int, Skv: int, causal: bool) -> int:
 
 
 def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, tile_q: int,
-                  tile_k: int, causal: bool, lam: float, scale: float, pot: bool = False):
+                  tile_k: int, causal: bool, lam: float, scale: float, pot: bool = False,
+                  block_mask_row: Optional[np.ndarray] = None):
     """One query tile of one head: returns (o_rows, lse_rows, mask[nkt], margin[nkt],
     ambiguous_fraction_rows or None).
 
     qh is the head's full query matrix [Sq][D]; kh, vh its kv head [Skv][D].  With
     pot=True kept tiles take Rowmax-PoT weights instead of exact exponentials.
+    block_mask_row, if given, is a boolean [nkt] of the key tiles this query tile visits.
     """
     Sq, Skv = qh.shape[0], kh.shape[0]
     nkt = (Skv + tile_k - 1) // tile_k
@@ -215,6 +219,8 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
     margin = np.full(nkt, np.inf)
     last_tile = last_visible_key(r1, Sq, Skv, causal) // tile_k
     for j in range(last_tile + 1):
+        if block_mask_row is not None and not block_mask_row[j]:
+            continue                       # not selected: not visited (mask stays -1)
         c0, c1 = j * tile_k, min((j + 1) * tile_k, Skv)
         s = _tile_logits(qrows, kh[c0:c1], scale, qpos, np.arange(c0, c1), causal)
         d = _row_gap(np.max(s, axis=1), m)
@@ -227,16 +233,21 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
             m, l, o, a = _online_update_pot(m, l, o, a, s, vh[c0:c1])
         else:
             m, l, o = _online_update(m, l, o, s, vh[c0:c1])
-    amb = a / l if pot else None
-    o, lse = _finish(m, l, o)
+    seen = l > 0.0                         # rows with at least one visited visible key
+    lsafe = np.where(seen, l, 1.0)
+    amb = np.where(seen, a / lsafe, 0.0) if pot else None
+    o, lse = _finish(m, lsafe, o)
+    o = np.where(seen[:, None], o, 0.0)
+    lse = np.where(seen, lse, NEG_INF)
     return o, lse, mask, margin, amb
 
 
 def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: float,
             tile_q: int, tile_k: int, scale: Optional[float] = None,
-            pot: bool = False) -> PrefillResult:
+            pot: bool = False, block_mask: Optional[np.ndarray] = None) -> PrefillResult:
     """Skip Softmax prefill over q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] (fp64); pot=True
-    uses Rowmax-PoT weights on kept tiles."""
+    uses Rowmax-PoT weights on kept tiles; block_mask, if given, is a boolean
+    [B][Hq][nqt][nkt] of the (query tile, key tile) pairs to visit."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     if Hq % Hkv or (causal and Sq > Skv):
@@ -255,9 +266,10 @@ def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: f
             kh, vh = k[b, h // G], v[b, h // G]
             for t in range(nqt):
                 r0, r1 = t * tile_q, min((t + 1) * tile_q, Sq)
-                ot, lt, mt, gt, at = prefill_qtile(q[b, h], kh, vh, t, tile_q=tile_q,
-                                                   tile_k=tile_k, causal=causal, lam=lam,
-                                                   scale=scale, pot=pot)
+                ot, lt, mt, gt, at = prefill_qtile(
+                    q[b, h], kh, vh, t, tile_q=tile_q, tile_k=tile_k, causal=causal, lam=lam,
+                    scale=scale, pot=pot,
+                    block_mask_row=None if block_mask is None else block_mask[b, h, t])
                 o[b, h, r0:r1], lse[b, h, r0:r1] = ot, lt
                 mask[b, h, t], margin[b, h, t] = mt, gt
                 if pot:

@@ -1,4 +1,4 @@
-"""Pins of the oracle's decode block mask ("NVIDIA Introduces Skip Softmax ...",
+"""Pins of the oracle's block mask, decode and prefill ("NVIDIA Introduces Skip Softmax ...",
 "Benefits and Implementation": Skip Softmax combined with another sparse-attention
 method).  Tiles outside the mask are not visited; the skip rule runs over the selected
 tiles of each split.  Checked against SDPA restricted to the selected keys (a library
@@ -142,3 +142,82 @@ def test_blockmask_mutants_are_caught(monkeypatch, fn):
         except (AssertionError, FloatingPointError, ValueError):
             caught += 1
     assert caught > 0
+
+
+# ---------------------------------------------------------------------------
+# prefill: a mask over (query tile, key tile) pairs
+# ---------------------------------------------------------------------------
+def test_worked_prefill_unselected_tile_not_in_running_max():
+    # one row of logits [9, 9 | 1, 0 | 2, -3] (D = 1, q = 1), tiles of 2 keys, non-causal.
+    # With key tile 0 unselected the running max before tile 2 is 1, tile 2's gap is +1:
+    # kept.  With every tile selected, tiles 1 and 2 have gaps 1 - 9 and 2 - 9, and
+    # lambda = e^-5 skips both.
+    q = np.ones((1, 1, 1, 1))
+    k = np.array([9.0, 9.0, 1.0, 0.0, 2.0, -3.0]).reshape(1, 1, 6, 1)
+    v = np.array([100.0, 100.0, 1.0, 2.0, 3.0, 4.0]).reshape(1, 1, 6, 1)
+    sel = np.array([False, True, True]).reshape(1, 1, 1, 3)
+    r = oracle.prefill(q, k, v, causal=False, lam=E(-5), tile_q=1, tile_k=2, scale=1.0,
+                       block_mask=sel)
+    assert r.mask[0, 0, 0].tolist() == [-1, 0, 0]
+    z = E(1) + E(0) + E(2) + E(-3)
+    assert abs(r.o[0, 0, 0, 0] - (E(1) + 2 + 3 * E(2) + 4 * E(-3)) / z) < 1e-14
+    r = oracle.prefill(q, k, v, causal=False, lam=E(-5), tile_q=1, tile_k=2, scale=1.0)
+    assert r.mask[0, 0, 0].tolist() == [0, 1, 1]
+
+
+def test_worked_prefill_row_without_selected_keys():
+    # causal Sq = Skv = 4, tiles 2 x 2: query tile 1 selects only key tile 1; its rows
+    # 2 and 3 see keys 2 and 2..3.  Query tile 0 selects nothing: output 0, lse -inf.
+    q = np.ones((1, 1, 4, 1))
+    k = np.array([5.0, 5.0, 0.0, 1.0]).reshape(1, 1, 4, 1)
+    v = np.array([9.0, 9.0, 1.0, 2.0]).reshape(1, 1, 4, 1)
+    sel = np.array([[False, False], [False, True]]).reshape(1, 1, 2, 2)
+    r = oracle.prefill(q, k, v, causal=True, lam=0.0, tile_q=2, tile_k=2, scale=1.0,
+                       block_mask=sel)
+    o = r.o[0, 0, :, 0]
+    assert o[0] == 0.0 and o[1] == 0.0 and np.all(r.lse[0, 0, :2] == -np.inf)
+    assert abs(o[2] - 1.0) < 1e-15
+    assert abs(o[3] - (1 * E(0) + 2 * E(1)) / (E(0) + E(1))) < 1e-14
+    assert r.mask[0, 0].tolist() == [[-1, -1], [-1, 0]]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("seed", range(3))
+def test_prefill_lambda0_equals_sdpa_on_selected_keys(causal, seed):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, Sq, Skv, D, tq, tk = 1, 2, 1, 11, 14, 8, 3, 4
+    q = rng.standard_normal((B, Hq, Sq, D))
+    k = rng.standard_normal((B, Hkv, Skv, D)) * 2
+    v = rng.standard_normal((B, Hkv, Skv, D))
+    nqt, nkt = -(-Sq // tq), -(-Skv // tk)
+    sel = rng.random((B, Hq, nqt, nkt)) < 0.6
+    r = oracle.prefill(q, k, v, causal=causal, lam=0.0, tile_q=tq, tile_k=tk,
+                       block_mask=sel)
+    for h in range(Hq):
+        rows_sel = np.repeat(np.repeat(sel[0, h], tq, axis=0)[:Sq], tk, axis=1)[:, :Skv]
+        from pins import causal_allowed
+        allowed = rows_sel & causal_allowed(Sq, Skv, causal)
+        has = allowed.any(axis=1)
+        want = sdpa(q[0, h][has], k[0, 0], v[0, 0], allowed[has], 1 / math.sqrt(D))
+        assert np.max(np.abs(r.o[0, h][has] - want)) < 1e-12
+        assert np.all(r.o[0, h][~has] == 0.0) and np.all(r.lse[0, h][~has] == -np.inf)
+
+
+def test_prefill_all_selected_equals_no_mask_and_unselected_keys_do_not_matter():
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 2, 12, 8))
+    k = rng.standard_normal((1, 1, 12, 8)) * 3
+    v = rng.standard_normal((1, 1, 12, 8))
+    a = oracle.prefill(q, k, v, causal=True, lam=0.05, tile_q=4, tile_k=4)
+    b = oracle.prefill(q, k, v, causal=True, lam=0.05, tile_q=4, tile_k=4,
+                       block_mask=np.ones((1, 2, 3, 3), dtype=bool))
+    assert np.array_equal(a.o, b.o) and np.array_equal(a.mask, b.mask)
+    # key tile 1 selected by no query tile: changing its keys and values changes nothing
+    sel = np.ones((1, 2, 3, 3), dtype=bool)
+    sel[:, :, :, 1] = False
+    c = oracle.prefill(q, k, v, causal=True, lam=0.05, tile_q=4, tile_k=4, block_mask=sel)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0, 4:8] += 40.0
+    v2[0, 0, 4:8] = 1e6
+    d = oracle.prefill(q, k2, v2, causal=True, lam=0.05, tile_q=4, tile_k=4, block_mask=sel)
+    assert np.array_equal(c.o, d.o) and np.array_equal(c.mask, d.mask)
