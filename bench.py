@@ -428,6 +428,28 @@ def run_ours(args):
             "max_abs_err_vs_bf16_lambda0": float(d.max()),
             "mean_abs_err_vs_bf16_lambda0": float(d.mean())})
     del q8, k8
+    # Skip Softmax behind a prefill block selector: a seeded mask keeps the diagonal and
+    # the first key tile of every query tile and half of the others at random
+    nqt_m = nqt
+    gm = torch.Generator(device="cpu").manual_seed(4321 + rank)
+    pm = torch.rand((wp.B, wp.Hq, nqt_m, nqt_m), generator=gm) < 0.5
+    ar = torch.arange(nqt_m)
+    pm[:, :, ar, ar] = True
+    pm[:, :, :, 0] = True
+    pm = pm.to(torch.uint8).to(dev)
+    causal_pairs = wp.B * wp.Hq * nqt_m * (nqt_m + 1) // 2
+    sel_pairs = int(torch.tril(pm.to(torch.int64)).sum().item())
+    sweep_pbm = []
+    for lam in (0.0, lam_pf[TARGET_RHO]):
+        def run_pbm():
+            bs.prefill(q, k, v, lam, causal=True, out=o, skip_counts=cnt, block_mask=pm)
+        sec = time_events(run_pbm, 3)
+        sk = int(cnt.sum().item())
+        sweep_pbm.append({
+            "lambda": lam, "selected_fraction": sel_pairs / causal_pairs,
+            "skip_ratio_of_selected": sk / sel_pairs, "ms": sec * 1e3,
+            "speedup_vs_unmasked_lambda0": t_dense / sec})
+    del pm
     del o_ref
     od_ref = None
     sweep_dec = []
@@ -579,7 +601,8 @@ def run_ours(args):
                    "hbm_frac_of_measured": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9
                    / peaks["hbm_gbs"], "skip_ratio": rho_dec, "lambda": lam_dec},
         "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot,
-                  "decode_block_mask": sweep_bm, "prefill_fp8_qk": sweep_fp8},
+                  "decode_block_mask": sweep_bm, "prefill_fp8_qk": sweep_fp8,
+                  "prefill_block_mask": sweep_pbm},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "roofline": roofline,

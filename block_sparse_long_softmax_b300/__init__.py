@@ -37,7 +37,8 @@ class PrefillOpts(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("lse", ctypes.c_void_p),
                 ("skip_mask", ctypes.c_void_p), ("visited_counts", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int),
-                ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float)]
+                ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float),
+                ("block_mask", ctypes.c_void_p)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
@@ -149,12 +150,13 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
             softmax_scale: float = 0.0, return_lse: bool = False, return_mask: bool = False,
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
             wait_limit_ms: int = 0, exp_mode: str = "exact",
-            qk_descale: float = 0.0) -> PrefillOut:
+            qk_descale: float = 0.0, block_mask=None) -> PrefillOut:
     """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
     q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
     Q.K^T in e4m3, scaled by qk_descale); v is bf16.  exp_mode "exact" uses exponentials on
-    kept tiles, "pot" Rowmax-PoT powers of two.
+    kept tiles, "pot" Rowmax-PoT powers of two.  block_mask: optional uint8/bool CUDA
+    tensor [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)] of the pairs to visit.
     """
     import torch
     lib = library()
@@ -171,9 +173,15 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     mask = torch.empty((B, Hq, nqt, nkt), dtype=torch.uint8, device=q.device) if return_mask else None
     vis = torch.empty(Hq, dtype=torch.int64, device=q.device) if return_visited else None
     ptr = lambda t: _P(t.data_ptr()) if t is not None else _P(0)  # noqa: E731
+    if block_mask is not None and (
+            not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda
+            or block_mask.dtype not in (torch.uint8, torch.bool)
+            or tuple(block_mask.shape) != (B, Hq, nqt, nkt) or not block_mask.is_contiguous()):
+        raise TypeError(f"block_mask must be a contiguous uint8/bool CUDA tensor "
+                        f"of shape {(B, Hq, nqt, nkt)}")
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
                        ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
-                       float(qk_descale))
+                       float(qk_descale), ptr(block_mask).value)
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))

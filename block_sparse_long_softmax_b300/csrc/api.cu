@@ -193,6 +193,7 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   set_lambda(lambda, &p.lam_log2, &p.lam_pos);
   p.qk_e4m3 = op.qk_format == 1 ? 1 : 0;
+  p.block_mask = op.block_mask;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = op.lse;
   p.skip_counts = reinterpret_cast<unsigned long long*>(skip_counts);

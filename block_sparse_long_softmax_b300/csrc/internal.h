@@ -72,6 +72,7 @@ struct PrefillParams {
   int lam_pos;
   int exp_mode;          // 0 exact exponentials, 1 Rowmax-PoT weights
   int qk_e4m3;           // Q and K are e4m3 (V stays bf16)
+  const uint8_t* block_mask;  // [B][Hq][nqt][nkt] pairs to visit, or null for all
   __nv_bfloat16* o;      // [B][Hq][Sq][D]
   float* lse;            // [B][Hq][Sq] or null
   unsigned long long* skip_counts;

@@ -350,6 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; x < 2; ++x) {
         TileRow& t = tr[x];
         if (j >= t.n) continue;
+        // caller's block mask: a (vote tile, key tile) pair outside it is not visited
+        bool sel0 = true, sel1 = true;  // vote groups 0 and 1 of this Q tile
+        if (p.block_mask) {
+          const int qt0 = (qrow0 + x * kQRows) / TQ;
+          const uint8_t* mcol = p.block_mask + (static_cast<size_t>(b) * p.Hq + hq) * p.nqt * p.nkt + j;
+          sel0 = mcol[static_cast<size_t>(qt0) * p.nkt] != 0;
+          sel1 = TQ == 128 ? sel0 : (qt0 + 1 < p.nqt && mcol[static_cast<size_t>(qt0 + 1) * p.nkt] != 0);
+        }
         const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
         const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
         if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
@@ -387,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // one vote group = the whole Q tile: a barrier that ANDs the row votes
           // (every warp does exactly one barrier operation per tile, so the warps
           // stay matched even when a bounded wait has given up)
-          const bool sk = p.lam_pos && named_bar_and(1 + x, 128, row_vote);
+          // (an unselected tile is the same for every warp: no barrier)
+          const bool sk = !sel0 || (p.lam_pos && named_bar_and(1 + x, 128, row_vote));
           skip_g[0] = skip_g[1] = sk;
         } else {
         const bool warp_vote = __all_sync(0xffffffffu, row_vote);
@@ -398,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // vote.  A 64-row group past its causal range never keeps the tile.  Every
         // warp does exactly one barrier operation per tile, so the warps stay
         // matched even when a bounded wait has given up.
-        const bool out_of_range = j >= (grp == 0 ? t.n_half0 : t.n_half1);
+        const bool out_of_range =
+            grp == 0 ? (j >= t.n_half0 || !sel0) : (j >= t.n_half1 || !sel1);
         if ((!warp_vote || !p.lam_pos) && !out_of_range) {
           named_bar_arrive(1 + x, 128);
           skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
@@ -406,14 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           named_bar_sync(1 + x, 128);
           const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
-          // tiles past a 64-row group's causal range are not visited by it
-          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
-          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
+          // tiles past a 64-row group's causal range, or outside the block mask, are
+          // not visited by it
+          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0 || !sel0;
+          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1 || !sel1;
         }
         }
         const bool any_kept = !(skip_g[0] && skip_g[1]);
         const bool my_skip = skip_g[grp];
-        if (r == grp * TQ && j < t.n_grp) {  // one thread per vote group records it
+        if (r == grp * TQ && j < t.n_grp && (grp == 0 ? sel0 : sel1)) {  // one thread per vote group records it
           ++n_visit;
           n_skip += my_skip ? 1 : 0;
           if (p.skip_mask)
@@ -449,8 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float la[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[BK / 2];
             if constexpr (!POT) {
-              // P = 2^(s*scale*log2e - R) in bf16, written over S
-              const float negR = -t.R;
+              // P = 2^(s*scale*log2e - R) in bf16, written over S (a row that has
+              // seen no key yet, R = -inf, only has masked keys here: P = 0)
+              const float negR = t.R == -INFINITY ? 0.f : -t.R;
 #pragma unroll
               for (int i = 0; i < BK / 2; ++i) {
                 float x0, x1;
@@ -473,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // in which the exponent's rounding is treated as ambiguous.
               const float ua = sl2 * (1.f / 127.f);
               const float ub = 1.f - t.M * (1.f / 127.f);
-              const float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
+              const float c = t.R == -INFINITY ? 0.f
+                                               : __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
 #pragma unroll
               for (int i = 0; i < BK / 2; ++i) {
                 const float u0 = sat_fma(__uint_as_float(sv[2 * i]), ua, ub);
@@ -519,19 +532,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ov[D];
         tmem_ld<D>(lane_base + (x == 0 ? C::kColO0 : C::kColO1), ov);
         if (t.valid && ok) {
-          const float inv = 1.f / t.l;
+          // a row with no visited visible key (block mask) has l = 0: output 0, LSE -inf
+          const bool seen = t.l > 0.f;
+          const float inv = seen ? 1.f / t.l : 0.f;
           __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row) * D;
           uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
           for (int i = 0; i < D / 8; ++i)
-            dst[i] = make_uint4(
+            dst[i] = seen ? make_uint4(
                 pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
+                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv))
+                          : make_uint4(0u, 0u, 0u, 0u);
           if (p.lse)
             p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row] =
-                (t.R + __log2f(t.l)) * 0.69314718055994531f;
+                seen ? (t.R + __log2f(t.l)) * 0.69314718055994531f : -INFINITY;
         }
       }
     }

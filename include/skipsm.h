@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 103
+#define SKIPSM_VERSION 104
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -102,6 +102,15 @@ typedef struct skipsm_prefill_opts {
                              fp32 accumulation, v, P and o stay bf16 */
   float qk_descale;       /* multiplies Q.K^T before the softmax scale (the product of the q and
                              k quantisation scales); 0 = 1 */
+  const uint8_t* block_mask; /* optional in, device [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)]:
+                             nonzero = visit the (vote tile, key tile) pair.  Skip Softmax
+                             combined with a prefill block selector ("NVIDIA Introduces Skip
+                             Softmax ...", "Benefits and Implementation"): an unselected pair
+                             takes no exponentials, no P.V, no vote and does not enter the
+                             running max (its Q.K^T is still computed when the other vote
+                             group or Q tile of the CTA needs the key tile); skip_mask reports
+                             it as 2; a row with no visible selected key gets o = 0 and
+                             lse = -inf.  NULL = every pair. */
 } skipsm_prefill_opts;
 
 /*
