@@ -106,7 +106,7 @@ __device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[
 template <>
 __device__ __forceinline__ void tmem_st<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8>
+template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8, bool BM>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= t.n) continue;
         // caller's block mask: a (vote tile, key tile) pair outside it is not visited
         bool sel0 = true, sel1 = true;  // vote groups 0 and 1 of this Q tile
-        if (p.block_mask) {
+        if constexpr (BM) {
           const int qt0 = (qrow0 + x * kQRows) / TQ;
           const uint8_t* mcol = p.block_mask + (static_cast<size_t>(b) * p.Hq + hq) * p.nqt * p.nkt + j;
           sel0 = mcol[static_cast<size_t>(qt0) * p.nkt] != 0;
@@ -395,8 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // one vote group = the whole Q tile: a barrier that ANDs the row votes
           // (every warp does exactly one barrier operation per tile, so the warps
           // stay matched even when a bounded wait has given up)
-          // (an unselected tile is the same for every warp: no barrier)
-          const bool sk = !sel0 || (p.lam_pos && named_bar_and(1 + x, 128, row_vote));
+          bool sk;
+          if constexpr (BM)  // an unselected tile is the same for every warp: no barrier
+            sk = !sel0 || (p.lam_pos && named_bar_and(1 + x, 128, row_vote));
+          else
+            sk = p.lam_pos && named_bar_and(1 + x, 128, row_vote);
           skip_g[0] = skip_g[1] = sk;
         } else {
         const bool warp_vote = __all_sync(0xffffffffu, row_vote);
@@ -407,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // vote.  A 64-row group past its causal range never keeps the tile.  Every
         // warp does exactly one barrier operation per tile, so the warps stay
         // matched even when a bounded wait has given up.
-        const bool out_of_range =
-            grp == 0 ? (j >= t.n_half0 || !sel0) : (j >= t.n_half1 || !sel1);
+        bool out_of_range = j >= (grp == 0 ? t.n_half0 : t.n_half1);
+        if constexpr (BM) out_of_range = out_of_range || !(grp == 0 ? sel0 : sel1);
         if ((!warp_vote || !p.lam_pos) && !out_of_range) {
           named_bar_arrive(1 + x, 128);
           skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
@@ -418,13 +421,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
           // tiles past a 64-row group's causal range, or outside the block mask, are
           // not visited by it
-          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0 || !sel0;
-          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1 || !sel1;
+          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
+          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
+          if constexpr (BM) {
+            skip_g[0] = skip_g[0] || !sel0;
+            skip_g[1] = skip_g[1] || !sel1;
+          }
         }
         }
         const bool any_kept = !(skip_g[0] && skip_g[1]);
         const bool my_skip = skip_g[grp];
-        if (r == grp * TQ && j < t.n_grp && (grp == 0 ? sel0 : sel1)) {  // one thread per vote group records it
+        bool counted = r == grp * TQ && j < t.n_grp;  // one thread per vote group records it
+        if constexpr (BM) counted = counted && (grp == 0 ? sel0 : sel1);
+        if (counted) {
           ++n_visit;
           n_skip += my_skip ? 1 : 0;
           if (p.skip_mask)
@@ -462,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (!POT) {
               // P = 2^(s*scale*log2e - R) in bf16, written over S (a row that has
               // seen no key yet, R = -inf, only has masked keys here: P = 0)
-              const float negR = t.R == -INFINITY ? 0.f : -t.R;
+              float negR = -t.R;
+              if constexpr (BM) negR = t.R == -INFINITY ? 0.f : negR;
 #pragma unroll
               for (int i = 0; i < BK / 2; ++i) {
                 float x0, x1;
@@ -485,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // in which the exponent's rounding is treated as ambiguous.
               const float ua = sl2 * (1.f / 127.f);
               const float ub = 1.f - t.M * (1.f / 127.f);
-              const float c = t.R == -INFINITY ? 0.f
-                                               : __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
+              float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
+              if constexpr (BM) c = t.R == -INFINITY ? 0.f : c;
 #pragma unroll
               for (int i = 0; i < BK / 2; ++i) {
                 const float u0 = sat_fma(__uint_as_float(sv[2 * i]), ua, ub);
@@ -532,22 +542,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ov[D];
         tmem_ld<D>(lane_base + (x == 0 ? C::kColO0 : C::kColO1), ov);
         if (t.valid && ok) {
-          // a row with no visited visible key (block mask) has l = 0: output 0, LSE -inf
-          const bool seen = t.l > 0.f;
-          const float inv = seen ? 1.f / t.l : 0.f;
+          float inv = 1.f / t.l;
           __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row) * D;
           uint4* dst = reinterpret_cast<uint4*>(orow);
+          float lse2 = t.R + __log2f(t.l);
+          if constexpr (BM) {
+            // a row with no visited visible key (block mask) has l = 0: output 0, LSE -inf
+            if (!(t.l > 0.f)) {
+#pragma unroll
+              for (int i = 0; i < D; ++i) ov[i] = 0u;
+              inv = 0.f;
+              lse2 = -INFINITY;
+            }
+          }
 #pragma unroll
           for (int i = 0; i < D / 8; ++i)
-            dst[i] = seen ? make_uint4(
+            dst[i] = make_uint4(
                 pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv))
-                          : make_uint4(0u, 0u, 0u, 0u);
+                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
           if (p.lse)
-            p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row] =
-                seen ? (t.R + __log2f(t.l)) * 0.69314718055994531f : -INFINITY;
+            p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row] = lse2 * 0.69314718055994531f;
         }
       }
     }
@@ -567,11 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8>
+template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8, bool BM>
 cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, BK, TQ, NK, NV, F8>;
-  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT, F8>;
+  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT, F8, BM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
@@ -583,18 +599,18 @@ cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const C
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, const PrefillParams& p, cudaStream_t stream) {
-#define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)                                     \
-  if (p.D == d && p.tile_k == bk && p.tile_q == tq && !p.qk_e4m3)                \
-    return p.exp_mode == 1 ? launch_cfg<d, bk, tq, nk, nv, true, false>(qmap, kmap, vmap, p, stream) \
-                           : launch_cfg<d, bk, tq, nk, nv, false, false>(qmap, kmap, vmap, p, stream);
-  // e4m3 Q and K: 128-row vote groups or 64, 128-key tiles, D = 128
-  if (p.qk_e4m3 && p.D == 128 && p.tile_k == 128) {
-    if (p.tile_q == 128)
-      return p.exp_mode == 1 ? launch_cfg<128, 128, 128, 4, 3, true, true>(qmap, kmap, vmap, p, stream)
-                             : launch_cfg<128, 128, 128, 4, 3, false, true>(qmap, kmap, vmap, p, stream);
-    return p.exp_mode == 1 ? launch_cfg<128, 128, 64, 4, 3, true, true>(qmap, kmap, vmap, p, stream)
-                           : launch_cfg<128, 128, 64, 4, 3, false, true>(qmap, kmap, vmap, p, stream);
+  // template flags: Rowmax-PoT weights, e4m3 Q/K, caller block mask
+#define SKIPSM_PREFILL_FLAGS(d, bk, tq, nk, nv, f8)                                           \
+  {                                                                                         \
+    const bool pot = p.exp_mode == 1, bm = p.block_mask != nullptr;                         \
+    if (pot && bm) return launch_cfg<d, bk, tq, nk, nv, true, f8, true>(qmap, kmap, vmap, p, stream);   \
+    if (pot) return launch_cfg<d, bk, tq, nk, nv, true, f8, false>(qmap, kmap, vmap, p, stream);        \
+    if (bm) return launch_cfg<d, bk, tq, nk, nv, false, f8, true>(qmap, kmap, vmap, p, stream);         \
+    return launch_cfg<d, bk, tq, nk, nv, false, f8, false>(qmap, kmap, vmap, p, stream);                \
   }
+#define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)                                 \
+  if (p.D == d && p.tile_k == bk && p.tile_q == tq && !p.qk_e4m3)          \
+    SKIPSM_PREFILL_FLAGS(d, bk, tq, nk, nv, false)
   SKIPSM_PREFILL_CASE(128, 128, 128, 3, 2)
   SKIPSM_PREFILL_CASE(128, 128, 64, 3, 2)
   SKIPSM_PREFILL_CASE(128, 64, 128, 4, 4)
@@ -603,7 +619,13 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
   SKIPSM_PREFILL_CASE(64, 128, 64, 4, 3)
   SKIPSM_PREFILL_CASE(64, 64, 128, 6, 6)
   SKIPSM_PREFILL_CASE(64, 64, 64, 6, 6)
+  // e4m3 Q and K: 128-row vote groups or 64, 128-key tiles, D = 128
+  if (p.qk_e4m3 && p.D == 128 && p.tile_k == 128) {
+    if (p.tile_q == 128) SKIPSM_PREFILL_FLAGS(128, 128, 128, 4, 3, true)
+    SKIPSM_PREFILL_FLAGS(128, 128, 64, 4, 3, true)
+  }
 #undef SKIPSM_PREFILL_CASE
+#undef SKIPSM_PREFILL_FLAGS
   return cudaErrorInvalidValue;
 }
 
