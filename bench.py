@@ -611,7 +611,7 @@ def run_ours(args):
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(PREFILL),
-                "kernel": "prefill_kernel<128,128,128,3,2>",
+                "kernel": "prefill_kernel<128,128,128,3,2,0,0,0>",
                 "peak_source": f"{src} bf16_tflops_sustained (cuBLAS, power-capped loop)",
                 "burst_peak": peaks.get("bf16_tflops"),
                 "frac_of_burst": achieved / peaks.get("bf16_tflops", peak),
