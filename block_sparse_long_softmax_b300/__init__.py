@@ -38,7 +38,7 @@ class PrefillOpts(ctypes.Structure):
                 ("skip_mask", ctypes.c_void_p), ("visited_counts", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int),
                 ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float),
-                ("block_mask", ctypes.c_void_p)]
+                ("block_mask", ctypes.c_void_p), ("inject_wait_timeout", ctypes.c_int)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
@@ -150,7 +150,8 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
             softmax_scale: float = 0.0, return_lse: bool = False, return_mask: bool = False,
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
             wait_limit_ms: int = 0, exp_mode: str = "exact",
-            qk_descale: float = 0.0, block_mask=None) -> PrefillOut:
+            qk_descale: float = 0.0, block_mask=None,
+            inject_wait_timeout: bool = False) -> PrefillOut:
     """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
     q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
@@ -181,7 +182,8 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
                         f"of shape {(B, Hq, nqt, nkt)}")
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
                        ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
-                       float(qk_descale), ptr(block_mask).value)
+                       float(qk_descale), ptr(block_mask).value,
+                       1 if inject_wait_timeout else 0)
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))

@@ -202,6 +202,7 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.status = status;
   p.wait_cycles = wait_cycles(op.wait_limit_ms);
   p.exp_mode = op.exp_mode;
+  p.inject_fault = op.inject_wait_timeout ? 1 : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

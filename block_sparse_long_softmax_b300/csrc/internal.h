@@ -26,6 +26,7 @@ enum WaitSite : int {
   kSitePrefillPFull = 22,
   kSitePrefillODone = 23,
   kSitePrefillDrain = 24,
+  kSitePrefillInjected = 25,
 };
 
 struct DecodeParams {
@@ -73,6 +74,7 @@ struct PrefillParams {
   int exp_mode;          // 0 exact exponentials, 1 Rowmax-PoT weights
   int qk_e4m3;           // Q and K are e4m3 (V stays bf16)
   const uint8_t* block_mask;  // [B][Hq][nqt][nkt] pairs to visit, or null for all
+  int inject_fault;      // test hook: the softmax warps wait on a barrier nothing arrives at
   __nv_bfloat16* o;      // [B][Hq][Sq][D]
   float* lse;            // [B][Hq][Sq] or null
   unsigned long long* skip_counts;

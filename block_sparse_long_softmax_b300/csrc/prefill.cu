@@ -54,8 +54,8 @@ struct PrefillCfg {
   static constexpr int kOffV = kOffK + NK * kKBytes;
   static constexpr int kOffBar = kOffV + NV * kVBytes;
   // barriers: qfull, kfull[NK], kempty[NK], vfull[NV], vempty[NV], sfull[2],
-  //           pfull[2], odone[2], final
-  static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 1;
+  //           pfull[2], odone[2], final, never (failure-detection test hook)
+  static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 2;
   static constexpr int kOffVote = kOffBar + kNBar * 8;       // [2 x][2 parity][4 warps] int
   static constexpr int kOffDec = kOffVote + 2 * 2 * 4 * 4;   // [2] int
   static constexpr int kOffTmem = kOffDec + 2 * 4;           // uint32
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pfull = [&](int x) { return bar0 + 8u * (3 + 2 * NK + 2 * NV + x); };
   auto odone = [&](int x) { return bar0 + 8u * (5 + 2 * NK + 2 * NV + x); };
   const uint32_t final_bar = bar0 + 8u * (7 + 2 * NK + 2 * NV);
+  const uint32_t never_bar = bar0 + 8u * (8 + 2 * NK + 2 * NV);  // nothing arrives here
   int* svote = reinterpret_cast<int*>(smem + C::kOffVote);
   volatile int* sdec = reinterpret_cast<volatile int*>(smem + C::kOffDec);
   uint32_t* stmem = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(odone(x), 1);
     }
     mbar_init(final_bar, 1);
+    mbar_init(never_bar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -344,6 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     unsigned long long n_skip = 0, n_visit = 0;
     bool ok = true;
+    if (p.inject_fault) {
+      // failure-detection test hook: a wait on a barrier nothing arrives at, with half
+      // the normal bound so that it is the wait reported; the CTA then winds down
+      const WaitCtx half{p.wait_cycles / 2, p.status, abort_flag};
+      ok = mbar_wait(never_bar, 0, half, kSitePrefillInjected);
+    }
     bool next_ready = false;  // the S of the next tile in this order is known to be complete
     for (int j = 0; j < nmax; ++j) {
 #pragma unroll

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 104
+#define SKIPSM_VERSION 105
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -111,6 +111,10 @@ typedef struct skipsm_prefill_opts {
                              group or Q tile of the CTA needs the key tile); skip_mask reports
                              it as 2; a row with no visible selected key gets o = 0 and
                              lse = -inf.  NULL = every pair. */
+  int inject_wait_timeout; /* failure-detection test hook: in every CTA the softmax warps first
+                              wait on a barrier nothing arrives at (half of wait_limit_ms); the
+                              kernel ends early, outputs are undefined and skipsm_check()
+                              reports site 25 */
 } skipsm_prefill_opts;
 
 /*

@@ -114,3 +114,15 @@ def test_prefill_on_side_stream_and_reuse_out():
         bs.prefill(q, k, v, 1e-3, out=o)
     s.synchronize()
     assert torch.equal(o, ref)
+
+
+def test_prefill_bounded_wait_reports_timeout():
+    """A wait that nothing satisfies ends with a status code, not a hang or trap."""
+    w = synth.WORKLOADS["prefill_32k_gqa8"].with_(B=1, Hq=2, Hkv=1, Sq=300, Skv=300, window=64)
+    q, k, v, _ = device_inputs(w)
+    bs.prefill(q, k, v, 1e-3, wait_limit_ms=20, inject_wait_timeout=True)
+    assert bs.check() == 25
+    assert bs.check() == 0  # cleared
+    # the context is still usable and results are correct again
+    q, k, v, out = _run(w, 1e-3)
+    _compare_heads(w, q, k, v, out, 1e-3, [(0, h) for h in range(w.Hq)])
