@@ -94,3 +94,11 @@ def test_decode_bounded_wait_reports_timeout():
     assert bs.check() == 0  # cleared
     # the context is still usable and results are correct again
     _run_and_compare(w, 1e-3, 1)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_decode_gqa_groups_full_length_sampled(G):
+    # every supported group size at a 32K cache, sampled groups
+    w = synth.WORKLOADS["decode_32k_gqa8"].with_(B=4, Hq=8 * G, Hkv=8)
+    for lam in (0.0, 1e-3, 1e-2):
+        _run_and_compare(w, lam, 0, groups=[(0, 0), (w.B - 1, w.Hkv - 1), (2, 5)])

@@ -126,3 +126,27 @@ def test_prefill_bounded_wait_reports_timeout():
     # the context is still usable and results are correct again
     q, k, v, out = _run(w, 1e-3)
     _compare_heads(w, q, k, v, out, 1e-3, [(0, h) for h in range(w.Hq)])
+
+
+MEDIUM = [
+    # larger shapes than SMALL, sampled: D=64 with every tile configuration, batch > 1,
+    # non-causal, and Sq < Skv at a few thousand keys
+    (dict(B=2, Hq=8, Hkv=2, Sq=4096, Skv=4096, D=64, window=256), 64, 64),
+    (dict(B=2, Hq=8, Hkv=2, Sq=4096, Skv=4096, D=64, window=256), 128, 128),
+    (dict(B=2, Hq=8, Hkv=2, Sq=4096, Skv=4096, D=64, window=256), 64, 128),
+    (dict(B=2, Hq=8, Hkv=2, Sq=4096, Skv=4096, D=64, window=256), 128, 64),
+    (dict(B=3, Hq=16, Hkv=4, Sq=3000, Skv=5000, D=128, window=512), 128, 128),
+    (dict(B=1, Hq=8, Hkv=1, Sq=4000, Skv=4000, D=128, window=512, causal=False), 128, 128),
+]
+
+
+@pytest.mark.parametrize("lam", [1e-3, 1e-2])
+@pytest.mark.parametrize("case", range(len(MEDIUM)))
+def test_prefill_parity_medium_sampled(case, lam):
+    over, tq, tk = MEDIUM[case]
+    w = synth.WORKLOADS["prefill_32k_gqa8"].with_(**over)
+    q, k, v, out = _run(w, lam, tq, tk)
+    nqt = -(-w.Sq // tq)
+    heads = [(0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 2)]
+    _compare_heads(w, q, k, v, out, lam, heads, qtiles=[0, nqt // 3, nqt - 1])
+    _check_counts(out)
