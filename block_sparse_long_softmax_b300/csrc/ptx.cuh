@@ -229,36 +229,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Warp-converged forms: every lane executes the instruction stream (so the
-// operands stay in uniform registers) and only the lane with `issue` != 0
-// issues the MMA / commit.
+// MMA issue from a converged warp: every lane executes the instruction stream
+// (so the operands stay in uniform registers) and only the lane with `issue` != 0
+// issues the MMA / commit.  elect_one() picks that lane.
 __device__ __forceinline__ uint32_t elect_one() {
   uint32_t e;
   asm volatile(
@@ -268,6 +241,7 @@ __device__ __forceinline__ uint32_t elect_one() {
       : "=r"(e));
   return e;
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 A and B (kind::f16), fp32 accumulate
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
@@ -276,6 +250,7 @@ __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem], bf16 A and B (kind::f16), fp32 accumulate
 __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
@@ -293,6 +268,7 @@ __device__ __forceinline__ void umma_ss_f8_w(uint32_t d_tmem, uint64_t adesc, ui
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
+// Arrive on `bar` once every tcgen05 operation issued so far by the issuing lane is done.
 __device__ __forceinline__ void umma_commit_w(uint32_t bar, uint32_t issue) {
   asm volatile(
       "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
