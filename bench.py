@@ -470,6 +470,24 @@ def run_ours(args):
             "speedup_vs_lambda0": t_dense_d / sec, "model_speedup_2_over_2_minus_rho": 2 / (2 - rho),
             "max_abs_err_vs_lambda0": e_max})
 
+    # split count: each split restarts its running max (its first tile is always kept), so
+    # more splits fill the GPU sooner but cap the skip ratio lower
+    sweep_splits = []
+    for ns in (16, 32, 64):
+        wsn = torch.empty(bs.decode_workspace_size(wd.B, wd.Hq, wd.Hkv, wd.Skv, wd.D, ns),
+                          dtype=torch.uint8, device=dev)
+        for lam in (0.0, lam_dec):
+            def run_ns():
+                bs.decode(qd, kd, vd, lam, num_splits=ns, workspace=wsn, out=od,
+                          skip_counts=cntd)
+            sec = time_events(run_ns, 20)
+            kept = nblk_d - int(cntd[:: wd.G].sum().item())
+            sweep_splits.append({
+                "splits": ns, "lambda": lam, "skip_ratio": 1 - kept / nblk_d, "us": sec * 1e6,
+                "hbm_gbs_on_bytes_read": decode_bytes(wd, kept, ns) / sec / 1e9,
+                "speedup_vs_default_lambda0": t_dense_d / sec})
+        del wsn
+
     # Skip Softmax behind a block selector: a seeded mask keeps the first and the last
     # 64 tiles of every group (sink and recent window) and half of the others at random
     nb = -(-wd.Skv // 64)
@@ -636,6 +654,7 @@ def run_ours(args):
                    "hbm_frac_of_measured": decode_bytes(wd, kept_dec, nsplit) / t_dec / 1e9
                    / peaks["hbm_gbs"], "skip_ratio": rho_dec, "lambda": lam_dec},
         "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot,
+                  "decode_splits": sweep_splits,
                   "decode_block_mask": sweep_bm, "prefill_fp8_qk": sweep_fp8,
                   "prefill_block_mask": sweep_pbm},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -90,7 +90,14 @@ void set_lambda(float lambda, float* lam_log2, int* lam_pos) {
 }
 
 constexpr int kDecodeBk = 64;
-constexpr int kDecodeTargetCtas = 148 * 2 * 4;
+// Default split count: split CTAs run in waves of kDecodeSms * kDecodeCtasPerSm (two
+// resident per SM at D = 128, bound by shared memory), and a wave that is only partly
+// filled costs nearly as much as a full one.  Each CTA also pays a start-up of about
+// kDecodeCtaStartTiles tile loads before its pipeline is full.
+constexpr int kDecodeSms = 148;
+constexpr int kDecodeCtasPerSm = 2;
+constexpr int kDecodeCtaStartTiles = 4;
+constexpr int kDecodeMaxDefaultSplits = kDecodeSms * kDecodeCtasPerSm * 8;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -230,11 +237,26 @@ int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested) {
   const int nblk = (Skv + kDecodeBk - 1) / kDecodeBk;
   int want = requested;
   if (want == 0) {
+    // The count with the least modelled time: waves x (tiles per split + start-up), the
+    // fewest splits on a tie.  Fewer splits also skip more: each split's first tile is
+    // always kept (its running max starts at -inf), and a split that has not yet seen
+    // the large logits of earlier keys keeps tiles a longer prefix would skip.  Splits
+    // hold at least 16 tiles.
     const long long items = static_cast<long long>(B) * Hkv;
-    want = static_cast<int>((kDecodeTargetCtas + items - 1) / items);
-    // at least 16 tiles per split: each split's first tile is always kept (its running
-    // max starts at -inf), so short splits would cap the skip ratio
-    want = std::min(want, std::max(1, nblk / 16));
+    const long long slots = static_cast<long long>(kDecodeSms) * kDecodeCtasPerSm;
+    const int hi = std::min(std::max(1, nblk / 16), kDecodeMaxDefaultSplits);
+    long long best = -1;
+    want = 1;
+    for (int s = 1; s <= hi; ++s) {
+      const int per = (nblk + s - 1) / s;
+      if ((nblk + per - 1) / per != s) continue;  // the same cut as a smaller count
+      const long long waves = (items * s + slots - 1) / slots;
+      const long long cost = waves * (per + kDecodeCtaStartTiles);
+      if (best < 0 || cost < best) {
+        best = cost;
+        want = s;
+      }
+    }
   }
   want = std::max(1, std::min(want, nblk));
   const int per = (nblk + want - 1) / want;

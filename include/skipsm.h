@@ -144,12 +144,14 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
 /* ------------------------------------------------------------------------ */
 
 /*
- * Number of KV splits a decode call uses when the caller asks for 0: enough
- * (b, kv head, split) work items to fill the GPU, each split at least 16 key
- * tiles of 64 (every split keeps its first tile, so short splits would cap the
- * skip ratio).  The key range is cut into ceil(nblk/splits)-tile splits, and
- * empty trailing splits are dropped, so the count returned here is the
- * effective one.  Returns 0 for invalid sizes.
+ * Number of KV splits a decode call uses when the caller asks for 0.  The
+ * (b, kv head, split) CTAs run in waves of 2 per SM on the 148 SMs; the default
+ * is the count with the least modelled time, waves x (tiles per split + a
+ * start-up of 4 tiles), taking the fewest splits on a tie and at least 16 key
+ * tiles of 64 per split (every split keeps its first tile and restarts its
+ * running max, so short splits cap the skip ratio).  The key range is cut into
+ * ceil(nblk/splits)-tile splits, and empty trailing splits are dropped, so the
+ * count returned here is the effective one.  Returns 0 for invalid sizes.
  */
 int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested);
 

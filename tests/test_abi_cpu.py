@@ -140,6 +140,22 @@ def test_split_geometry_matches_oracle(lib, B, Hkv, Skv, req):
         assert ns <= max(1, nblk)
 
 
+@pytest.mark.parametrize("B,Hkv,Skv,want", [
+    # 64 (b, kv head) items x 9 splits = 576 CTAs: two nearly full waves of 296
+    (8, 8, 131072, 9),
+    # 128 items x 9 = 1152 CTAs: four nearly full waves
+    (16, 8, 32768, 9),
+    # few items: as many splits as 16-tile splits allow, all in one wave
+    (1, 1, 131072, 128),
+    (1, 8, 32768, 32),
+])
+def test_default_splits_fill_whole_waves(lib, B, Hkv, Skv, want):
+    ns = bs.decode_num_splits(B, Hkv, Skv, 0)
+    assert ns == want
+    nblk = -(-Skv // 64)
+    assert -(-nblk // ns) >= 16
+
+
 def test_workspace_size(lib):
     ns = bs.decode_num_splits(8, 8, 131072, 0)
     rows = 8 * 64 * ns
