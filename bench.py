@@ -197,7 +197,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("prefill.cu", "ptx.cuh", "internal.h"):
+    for f in ("prefill.cu", "ptx.cuh", "tmem_wide.cuh", "internal.h"):
         h.update(open(os.path.join(ROOT, "block_sparse_long_softmax_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 105
+#define SKIPSM_VERSION 106
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,

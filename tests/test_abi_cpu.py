@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.skipsm_version() == 105
+    assert lib.skipsm_version() == 106
 
 
 P = 0x10000  # a 16-byte aligned fake device address; validation never dereferences it
