@@ -561,40 +561,46 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hqd, hkd, hvd))
     d2h = ho.numel() * 2 + hod.numel() * 2 + 2 * wp.Hq * 8
 
-    # Copies run on their own streams and overlap the kernels of the same step: the
-    # decode's inputs go up while the prefill runs, the prefill's output comes down
-    # while the decode runs, and the next step's prefill inputs go up as soon as this
-    # step's prefill has read its own.  Every step still moves all of its inputs up
-    # and all of its outputs down inside the timed region.
+    # Copies run on their own streams and overlap the kernels.  The prefill's inputs,
+    # output and counts are double-buffered on the device, so the next step's prefill
+    # inputs go up and this step's output comes down while this step's prefill runs;
+    # the decode's inputs go up during the prefill of the same step.  Every step still
+    # moves all of its inputs up and all of its outputs down inside the timed region.
     main = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bufs = [(q, k, v, o, cnt),
+            (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o),
+             torch.empty_like(cnt))]
     hcnt = torch.empty_like(cnt, device="cpu").pin_memory()
     hcntd = torch.empty_like(cntd, device="cpu").pin_memory()
-    ev = {n: torch.cuda.Event() for n in ("in_pf", "in_dec", "pf_done", "dec_done",
-                                           "o_down", "od_down")}
+    ev_in_pf = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_pf_done = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_o_down = [torch.cuda.Event(), torch.cuda.Event()]
+    ev = {n: torch.cuda.Event() for n in ("in_dec", "dec_done", "od_down")}
 
     def e2e_step(i):
-        s_in.wait_event(ev["pf_done"])       # previous prefill has read q, k, v
+        bq, bk, bv, bo, bc = bufs[i % 2]
+        s_in.wait_event(ev_pf_done[i % 2])   # the prefill two steps back has read this set
         with torch.cuda.stream(s_in):
-            q.copy_(hq_, non_blocking=True)
-            k.copy_(hk_, non_blocking=True)
-            v.copy_(hv_, non_blocking=True)
-            ev["in_pf"].record(s_in)
-        main.wait_event(ev["in_pf"])
-        main.wait_event(ev["o_down"])        # previous output has left the device
-        run_prefill(lam_step)
-        ev["pf_done"].record(main)
+            bq.copy_(hq_, non_blocking=True)
+            bk.copy_(hk_, non_blocking=True)
+            bv.copy_(hv_, non_blocking=True)
+            ev_in_pf[i % 2].record(s_in)
+        main.wait_event(ev_in_pf[i % 2])
+        main.wait_event(ev_o_down[i % 2])    # the output two steps back has left the device
+        bs.prefill(bq, bk, bv, lam_step, causal=True, out=bo, skip_counts=bc)
+        ev_pf_done[i % 2].record(main)
         s_in.wait_event(ev["dec_done"])      # previous decode has read its inputs
         with torch.cuda.stream(s_in):
             qd.copy_(hqd, non_blocking=True)
             kd.copy_(hkd, non_blocking=True)
             vd.copy_(hvd, non_blocking=True)
             ev["in_dec"].record(s_in)
-        s_out.wait_event(ev["pf_done"])
+        s_out.wait_event(ev_pf_done[i % 2])
         with torch.cuda.stream(s_out):
-            ho.copy_(o, non_blocking=True)
-            hcnt.copy_(cnt, non_blocking=True)
-            ev["o_down"].record(s_out)
+            ho.copy_(bo, non_blocking=True)
+            hcnt.copy_(bc, non_blocking=True)
+            ev_o_down[i % 2].record(s_out)
         main.wait_event(ev["in_dec"])
         main.wait_event(ev["od_down"])
         run_decode(lam_dec)
@@ -605,9 +611,10 @@ def run_ours(args):
             hcntd.copy_(cntd, non_blocking=True)
             ev["od_down"].record(s_out)
 
-    e2e_steps = max(1, min(args.steps, 3))
+    e2e_steps = max(1, args.steps)
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_step(0)
+    e2e_step(1)
     torch.cuda.synchronize()
     barrier(pg_on)
     ea.record()
@@ -620,6 +627,7 @@ def run_ours(args):
     eb.record()
     torch.cuda.synchronize()
     e_sec = reduce_max(ea.elapsed_time(eb) / 1e3, pg_on, dev)
+    del bufs
     e2e_value = ws * e2e_steps * step_flops / e_sec / 1e12
 
     # ---- roofline of the dominant kernel (prefill, tensor-bound)
