@@ -27,6 +27,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -132,14 +133,18 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir=None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        if log_dir:
+            self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"skipsm_clocks{gpu_index}_", suffix=".csv")
+            os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(self.path) or ".", exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -540,7 +545,7 @@ def run_ours(args):
         return sum(a.elapsed_time(b) for a, b in ev_pf) / 1e3 + \
             sum(a.elapsed_time(b) for a, b in ev_dec) / 1e3
 
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clock_log) as clk:
         sec, wall = timed_loop(step, args.steps, 0, torch.cuda.synchronize, elapsed, pg_on, dev)
     clocks = clk.summary()
     t_pf = sum(a.elapsed_time(b) for a, b in ev_pf) / 1e3 / args.steps
@@ -773,6 +778,9 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=4.0,
                     help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="directory for the raw nvidia-smi samples of the timed region "
+                         "(clocks_rank<N>.csv); default: a temporary file")
     ap.add_argument("--kernel-only", choices=("prefill", "decode"),
                     help="only launch this kernel on --workload (for profiler captures)")
     ap.add_argument("--workload", default=PREFILL)
