@@ -293,8 +293,12 @@ def run_reference(args):
         return 0
     total_f, total_s = 0.0, 0.0
     desc = ""
+    import block_sparse_long_softmax_b300 as bs  # host-only query: the split geometry
+    import synth
+    wd = synth.WORKLOADS[DECODE]
+    splits = bs.decode_num_splits(wd.B, wd.Hkv, wd.Skv, 0)  # the same split geometry as ours
     for i in range(args.warmup + args.steps):
-        f, s, desc = oracle_sample(args.ref_budget, 1e-3, 1e-3, 16, seed_off=i % 3)
+        f, s, desc = oracle_sample(args.ref_budget, 1e-3, 1e-3, splits, seed_off=i % 3)
         if i >= args.warmup:
             total_f += f
             total_s += s
