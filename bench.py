@@ -272,7 +272,7 @@ def oracle_sample(budget_s: float, lam_pf: float, lam_dec: float, splits: int, s
     flops += 4.0 * 8 * wd.D * wd.Skv
     nqt = wp.Sq // 128
     t = nqt - 1
-    while sec < budget_s and t >= 0:
+    while (sec < budget_s or not tiles) and t >= 0:  # at least one query tile
         t0 = time.perf_counter()
         oracle.prefill_qtile(qh, kh, vh, t, tile_q=128, tile_k=128, causal=True, lam=lam_pf,
                              scale=1.0 / math.sqrt(wp.D))

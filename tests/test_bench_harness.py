@@ -81,3 +81,14 @@ def test_reference_arm_non_zero_rank_exits_quietly(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_oracle_line(capsys):
+    # the reference arm times the oracle on the host: one JSON line, no GPU needed
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0",
+                       "--ref-budget", "0.01"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert "9 splits" in line["config"]["sample_per_step"]
