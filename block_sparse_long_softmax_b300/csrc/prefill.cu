@@ -99,6 +99,14 @@ __device__ __forceinline__ void tmem_ld<64>(uint32_t taddr, uint32_t (&r)[64]) {
 template <>
 __device__ __forceinline__ void tmem_ld<128>(uint32_t taddr, uint32_t (&r)[128]) { tmem_ld128(taddr, r); }
 
+// the S row and its maximum over the tile's columns, in one load
+template <int N>
+__device__ __forceinline__ float tmem_ld_max(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ float tmem_ld_max<64>(uint32_t taddr, uint32_t (&r)[64]) { return tmem_ld64_max(taddr, r); }
+template <>
+__device__ __forceinline__ float tmem_ld_max<128>(uint32_t taddr, uint32_t (&r)[128]) { return tmem_ld128_max(taddr, r); }
+
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
 template <>
@@ -385,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
         tc_fence_after();
         uint32_t sv[BK];
-        tmem_ld<BK>(tS, sv);
+        // the load also returns the row's maximum over the tile (tcgen05.ld.red)
+        float mx = tmem_ld_max<BK>(tS, sv);
         const int key0 = j * BK;
         // tile-level (warp-uniform) test: does any row of this warp see a masked key?
         if (j >= t.j_mask) {
@@ -395,20 +404,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool masked = (p.causal && key > t.qpos) || key >= p.Skv;
             sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
           }
+          // the maximum over the visible keys: 16 independent chains, then a tree
+          float m16[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
+#pragma unroll
+          for (int i = 16; i < BK; i += 16)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
+          mx = m16[0];
         }
-        // 16 independent max chains, then a tree (short dependency chains)
-        float m16[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
-#pragma unroll
-        for (int i = 16; i < BK; i += 16)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
-        const float mx = m16[0];
         const float mt2 = t.valid ? mx * sl2 : -INFINITY;
         const float d = gapf(mt2, t.M);
         const bool row_vote = !t.valid || d < p.lam_log2;
