@@ -375,192 +375,216 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(never_bar, 0, half, kSitePrefillInjected);
     }
     bool next_ready = false;  // the S of the next tile in this order is known to be complete
-    for (int j = 0; j < nmax; ++j) {
+    // The softmax of one (Q tile x, key tile j): t is the row state of Q tile x, o that of the
+    // other Q tile.
+    auto softmax_tile = [&](TileRow& t, const TileRow& o, const int x, const int j) {
+      if (j >= t.n) return;
+      // caller's block mask: a (vote tile, key tile) pair outside it is not visited
+      bool sel0 = true, sel1 = true;  // vote groups 0 and 1 of this Q tile
+      if constexpr (BM) {
+        const int qt0 = (qrow0 + x * kQRows) / TQ;
+        const uint8_t* mcol = p.block_mask + (static_cast<size_t>(b) * p.Hq + hq) * p.nqt * p.nkt + j;
+        sel0 = mcol[static_cast<size_t>(qt0) * p.nkt] != 0;
+        sel1 = TQ == 128 ? sel0 : (qt0 + 1 < p.nqt && mcol[static_cast<size_t>(qt0 + 1) * p.nkt] != 0);
+      }
+      const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
+      const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
+      if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
+      tc_fence_after();
+      uint32_t sv[BK];
+      // the load also returns the row's maximum over the tile (tcgen05.ld.red)
+      float mx = tmem_ld_max<BK>(tS, sv);
+      const int key0 = j * BK;
+      // tile-level (warp-uniform) test: does any row of this warp see a masked key?
+      if (j >= t.j_mask) {
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        TileRow& t = tr[x];
-        if (j >= t.n) continue;
-        // caller's block mask: a (vote tile, key tile) pair outside it is not visited
-        bool sel0 = true, sel1 = true;  // vote groups 0 and 1 of this Q tile
+        for (int i = 0; i < BK; ++i) {
+          const int key = key0 + i;
+          const bool masked = (p.causal && key > t.qpos) || key >= p.Skv;
+          sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
+        }
+        // the maximum over the visible keys: 16 independent chains, then a tree
+        float m16[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
+#pragma unroll
+        for (int i = 16; i < BK; i += 16)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
+        mx = m16[0];
+      }
+      const float mt2 = t.valid ? mx * sl2 : -INFINITY;
+      const float d = gapf(mt2, t.M);
+      const bool row_vote = !t.valid || d < p.lam_log2;
+      bool skip_g[2];
+      if (TQ == 128) {
+        // one vote group = the whole Q tile: a barrier that ANDs the row votes
+        // (every warp does exactly one barrier operation per tile, so the warps
+        // stay matched even when a bounded wait has given up)
+        bool sk;
+        if constexpr (BM)  // an unselected tile is the same for every warp: no barrier
+          sk = !sel0 || (p.lam_pos && named_bar_and(1 + x, 128, row_vote));
+        else
+          sk = p.lam_pos && named_bar_and(1 + x, 128, row_vote);
+        skip_g[0] = skip_g[1] = sk;
+      } else {
+      const bool warp_vote = __all_sync(0xffffffffu, row_vote);
+      volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
+      if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
+      // A warp with a row that keeps the tile knows its vote group keeps it, so it
+      // only arrives on the barrier; warps whose rows all vote skip wait for every
+      // vote.  A 64-row group past its causal range never keeps the tile.  Every
+      // warp does exactly one barrier operation per tile, so the warps stay
+      // matched even when a bounded wait has given up.
+      bool out_of_range = j >= (grp == 0 ? t.n_half0 : t.n_half1);
+      if constexpr (BM) out_of_range = out_of_range || !(grp == 0 ? sel0 : sel1);
+      if ((!warp_vote || !p.lam_pos) && !out_of_range) {
+        named_bar_arrive(1 + x, 128);
+        // this group keeps the tile; the other group's decision is not needed (written
+        // with selects: an index by the warp's group would put skip_g in local memory)
+        skip_g[0] = grp != 0;
+        skip_g[1] = grp == 0;
+      } else {
+        named_bar_sync(1 + x, 128);
+        const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
+        // tiles past a 64-row group's causal range, or outside the block mask, are
+        // not visited by it
+        skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
+        skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
         if constexpr (BM) {
-          const int qt0 = (qrow0 + x * kQRows) / TQ;
-          const uint8_t* mcol = p.block_mask + (static_cast<size_t>(b) * p.Hq + hq) * p.nqt * p.nkt + j;
-          sel0 = mcol[static_cast<size_t>(qt0) * p.nkt] != 0;
-          sel1 = TQ == 128 ? sel0 : (qt0 + 1 < p.nqt && mcol[static_cast<size_t>(qt0 + 1) * p.nkt] != 0);
+          skip_g[0] = skip_g[0] || !sel0;
+          skip_g[1] = skip_g[1] || !sel1;
         }
-        const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
-        const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
-        if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
-        tc_fence_after();
-        uint32_t sv[BK];
-        // the load also returns the row's maximum over the tile (tcgen05.ld.red)
-        float mx = tmem_ld_max<BK>(tS, sv);
-        const int key0 = j * BK;
-        // tile-level (warp-uniform) test: does any row of this warp see a masked key?
-        if (j >= t.j_mask) {
-#pragma unroll
-          for (int i = 0; i < BK; ++i) {
-            const int key = key0 + i;
-            const bool masked = (p.causal && key > t.qpos) || key >= p.Skv;
-            sv[i] = masked ? __float_as_uint(-INFINITY) : sv[i];
+      }
+      }
+      const bool any_kept = !(skip_g[0] && skip_g[1]);
+      const bool my_skip = grp == 0 ? skip_g[0] : skip_g[1];
+      bool counted = r == grp * TQ && j < t.n_grp;  // one thread per vote group records it
+      if constexpr (BM) counted = counted && (grp == 0 ? sel0 : sel1);
+      if (counted) {
+        ++n_visit;
+        n_skip += my_skip ? 1 : 0;
+        if (p.skip_mask)
+          p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + t.qtile) * p.nkt + j] =
+              my_skip ? 1 : 0;
+      }
+      if (r == 0) sdec[x] = any_kept ? 1 : 0;
+      if (any_kept) {
+        if (!my_skip) {
+          t.M = fmaxf(t.M, mt2);
+          float alpha = 1.f;
+          bool resc = false;
+          if (t.M > t.R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
+            resc = t.R != -INFINITY;
+            alpha = ex2(t.R - t.M);
+            t.l *= alpha;
+            t.R = t.M;
           }
-          // the maximum over the visible keys: 16 independent chains, then a tree
-          float m16[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) m16[k] = __uint_as_float(sv[k]);
-#pragma unroll
-          for (int i = 16; i < BK; i += 16)
-#pragma unroll
-            for (int k = 0; k < 16; ++k) m16[k] = fmaxf(m16[k], __uint_as_float(sv[i + k]));
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-            for (int k = 0; k < w; ++k) m16[k] = fmaxf(m16[k], m16[k + w]);
-          mx = m16[0];
-        }
-        const float mt2 = t.valid ? mx * sl2 : -INFINITY;
-        const float d = gapf(mt2, t.M);
-        const bool row_vote = !t.valid || d < p.lam_log2;
-        bool skip_g[2];
-        if (TQ == 128) {
-          // one vote group = the whole Q tile: a barrier that ANDs the row votes
-          // (every warp does exactly one barrier operation per tile, so the warps
-          // stay matched even when a bounded wait has given up)
-          bool sk;
-          if constexpr (BM)  // an unselected tile is the same for every warp: no barrier
-            sk = !sel0 || (p.lam_pos && named_bar_and(1 + x, 128, row_vote));
-          else
-            sk = p.lam_pos && named_bar_and(1 + x, 128, row_vote);
-          skip_g[0] = skip_g[1] = sk;
-        } else {
-        const bool warp_vote = __all_sync(0xffffffffu, row_vote);
-        volatile int* vote = svote + (x * 2 + (j & 1)) * 4;
-        if (lane == 0) vote[wq] = warp_vote ? 1 : 0;
-        // A warp with a row that keeps the tile knows its vote group keeps it, so it
-        // only arrives on the barrier; warps whose rows all vote skip wait for every
-        // vote.  A 64-row group past its causal range never keeps the tile.  Every
-        // warp does exactly one barrier operation per tile, so the warps stay
-        // matched even when a bounded wait has given up.
-        bool out_of_range = j >= (grp == 0 ? t.n_half0 : t.n_half1);
-        if constexpr (BM) out_of_range = out_of_range || !(grp == 0 ? sel0 : sel1);
-        if ((!warp_vote || !p.lam_pos) && !out_of_range) {
-          named_bar_arrive(1 + x, 128);
-          skip_g[0] = skip_g[1] = true;  // the other group's decision is not needed
-          skip_g[grp] = false;
-        } else {
-          named_bar_sync(1 + x, 128);
-          const int v0 = vote[0], v1 = vote[1], v2 = vote[2], v3 = vote[3];
-          // tiles past a 64-row group's causal range, or outside the block mask, are
-          // not visited by it
-          skip_g[0] = (p.lam_pos && (v0 & v1 & 1)) || j >= t.n_half0;
-          skip_g[1] = (p.lam_pos && (v2 & v3 & 1)) || j >= t.n_half1;
-          if constexpr (BM) {
-            skip_g[0] = skip_g[0] || !sel0;
-            skip_g[1] = skip_g[1] || !sel1;
-          }
-        }
-        }
-        const bool any_kept = !(skip_g[0] && skip_g[1]);
-        const bool my_skip = skip_g[grp];
-        bool counted = r == grp * TQ && j < t.n_grp;  // one thread per vote group records it
-        if constexpr (BM) counted = counted && (grp == 0 ? sel0 : sel1);
-        if (counted) {
-          ++n_visit;
-          n_skip += my_skip ? 1 : 0;
-          if (p.skip_mask)
-            p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + t.qtile) * p.nkt + j] =
-                my_skip ? 1 : 0;
-        }
-        if (r == 0) sdec[x] = any_kept ? 1 : 0;
-        if (any_kept) {
-          if (!my_skip) {
-            t.M = fmaxf(t.M, mt2);
-            float alpha = 1.f;
-            bool resc = false;
-            if (t.M > t.R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
-              resc = t.R != -INFINITY;
-              alpha = ex2(t.R - t.M);
-              t.l *= alpha;
-              t.R = t.M;
-            }
-            if (__any_sync(0xffffffffu, resc)) {
-              // Every earlier P.V of this Q tile is complete: the S of this tile was
-              // committed after it, and the next P.V waits for this warpgroup.
+          if (__any_sync(0xffffffffu, resc)) {
+            // Every earlier P.V of this Q tile is complete: the S of this tile was
+            // committed after it, and the next P.V waits for this warpgroup.
 
-              // 32 columns at a time: the S row is still live in registers
+            // 32 columns at a time: the S row is still live in registers
 #pragma unroll 1
-              for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(tO + c0, ov);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c0, ov);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                tmem_st32(tO + c0, ov);
-              }
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c0, ov);
             }
-            float la[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[BK / 2];
-            if constexpr (!POT) {
-              // P = 2^(s*scale*log2e - R) in bf16, written over S (a row that has
-              // seen no key yet, R = -inf, only has masked keys here: P = 0)
-              float negR = -t.R;
-              if constexpr (BM) negR = t.R == -INFINITY ? 0.f : negR;
-#pragma unroll
-              for (int i = 0; i < BK / 2; ++i) {
-                float x0, x1;
-                ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negR);
-                const float e0 = ex2(x0), e1 = ex2(x1);
-                fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
-                pk[i] = pack_bf16x2(e0, e1);
-              }
-            } else {
-              // Rowmax-PoT ("Approximating Softmax in Pretrained LLMs ...", Abstract):
-              // the weight is 2^n, n = round(x), x = s*scale*log2e - M, anchored at the
-              // running row max M, and 0 below 2^-126.5.  One saturating FMA gives
-              // u = clamp(1 + x/127, 0, 1) (masked keys, -inf, give 0); adding
-              // 1.5*2^23 - 127 to 127*u rounds x to n (ties to even) and leaves the fp32
-              // bits 0x4B400000 + n; shifting those bits by 23 and adding the bits of
-              // 1.0 builds the fp32 bits of 2^n (n = -127 gives 0).  The factor
-              // 2^(M - R) to the accumulator's reference R is rounded to bf16, so
-              // P = 2^n * c is exact in bf16 and the row sum adds exactly what the MMA
-              // multiplies.  The fp32 error of x is below 3e-5, well inside the band
-              // in which the exponent's rounding is treated as ambiguous.
-              const float ua = sl2 * (1.f / 127.f);
-              const float ub = 1.f - t.M * (1.f / 127.f);
-              float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
-              if constexpr (BM) c = t.R == -INFINITY ? 0.f : c;
-#pragma unroll
-              for (int i = 0; i < BK / 2; ++i) {
-                const float u0 = sat_fma(__uint_as_float(sv[2 * i]), ua, ub);
-                const float u1 = sat_fma(__uint_as_float(sv[2 * i + 1]), ua, ub);
-                float y0, y1;
-                ffma2(y0, y1, u0, u1, 127.f, 12582912.f - 127.f);
-                const float p0 = __uint_as_float(__float_as_uint(y0) * 8388608u + 0x3F800000u);
-                const float p1 = __uint_as_float(__float_as_uint(y1) * 8388608u + 0x3F800000u);
-                float e0, e1;
-                ffma2(e0, e1, p0, p1, c, 0.f);
-                fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
-                pk[i] = pack_bf16x2(e0, e1);
-              }
-            }
-            t.l += (la[0] + la[1]) + (la[2] + la[3]);
-            tmem_st<BK / 2>(tS, pk);
-          } else {
-            uint32_t z[BK / 2];
-#pragma unroll
-            for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
-            tmem_st<BK / 2>(tS, z);
           }
+          float la[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[BK / 2];
+          if constexpr (!POT) {
+            // P = 2^(s*scale*log2e - R) in bf16, written over S (a row that has
+            // seen no key yet, R = -inf, only has masked keys here: P = 0)
+            float negR = -t.R;
+            if constexpr (BM) negR = t.R == -INFINITY ? 0.f : negR;
+#pragma unroll
+            for (int i = 0; i < BK / 2; ++i) {
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, negR);
+              const float e0 = ex2(x0), e1 = ex2(x1);
+              fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
+              pk[i] = pack_bf16x2(e0, e1);
+            }
+          } else {
+            // Rowmax-PoT ("Approximating Softmax in Pretrained LLMs ...", Abstract):
+            // the weight is 2^n, n = round(x), x = s*scale*log2e - M, anchored at the
+            // running row max M, and 0 below 2^-126.5.  One saturating FMA gives
+            // u = clamp(1 + x/127, 0, 1) (masked keys, -inf, give 0); adding
+            // 1.5*2^23 - 127 to 127*u rounds x to n (ties to even) and leaves the fp32
+            // bits 0x4B400000 + n; shifting those bits by 23 and adding the bits of
+            // 1.0 builds the fp32 bits of 2^n (n = -127 gives 0).  The factor
+            // 2^(M - R) to the accumulator's reference R is rounded to bf16, so
+            // P = 2^n * c is exact in bf16 and the row sum adds exactly what the MMA
+            // multiplies.  The fp32 error of x is below 3e-5, well inside the band
+            // in which the exponent's rounding is treated as ambiguous.
+            const float ua = sl2 * (1.f / 127.f);
+            const float ub = 1.f - t.M * (1.f / 127.f);
+            float c = __bfloat162float(__float2bfloat16_rn(ex2(t.M - t.R)));
+            if constexpr (BM) c = t.R == -INFINITY ? 0.f : c;
+#pragma unroll
+            for (int i = 0; i < BK / 2; ++i) {
+              const float u0 = sat_fma(__uint_as_float(sv[2 * i]), ua, ub);
+              const float u1 = sat_fma(__uint_as_float(sv[2 * i + 1]), ua, ub);
+              float y0, y1;
+              ffma2(y0, y1, u0, u1, 127.f, 12582912.f - 127.f);
+              const float p0 = __uint_as_float(__float_as_uint(y0) * 8388608u + 0x3F800000u);
+              const float p1 = __uint_as_float(__float_as_uint(y1) * 8388608u + 0x3F800000u);
+              float e0, e1;
+              ffma2(e0, e1, p0, p1, c, 0.f);
+              fadd2_acc(la[2 * (i & 1)], la[2 * (i & 1) + 1], e0, e1);
+              pk[i] = pack_bf16x2(e0, e1);
+            }
+          }
+          t.l += (la[0] + la[1]) + (la[2] + la[3]);
+          tmem_st<BK / 2>(tS, pk);
+        } else {
+          uint32_t z[BK / 2];
+#pragma unroll
+          for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
+          tmem_st<BK / 2>(tS, z);
         }
-        {
-          // Probe the next tile's S without blocking; its latency overlaps the
-          // fence and arrive below, and a complete phase skips the wait.
-          int xn = 1 - x, jn = x == 0 ? j : j + 1, nn = tr[1 - x].n;
-          if (jn >= nn) { xn = x; jn = j + 1; nn = t.n; }
-          next_ready = jn < nn && mbar_test_wait(sfull(xn), jn & 1);
+      }
+      {
+        // Probe the next tile's S without blocking; its latency overlaps the
+        // fence and arrive below, and a complete phase skips the wait.
+        int xn = 1 - x, jn = x == 0 ? j : j + 1, nn = o.n;
+        if (jn >= nn) { xn = x; jn = j + 1; nn = t.n; }
+        next_ready = jn < nn && mbar_test_wait(sfull(xn), jn & 1);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull(x));
+    };
+    if constexpr (POT) {
+      // One copy of the longer Rowmax-PoT body serves both Q tiles (x at run time, the row
+      // states swapping places): held once in the instruction caches it measured 17 % faster
+      // than two copies with a constant x, which the exact and FP8 bodies prefer (4-9 %).
+      TileRow ta = tr[0], tb = tr[1];
+#pragma unroll 1
+      for (int hs = 0; hs < 2 * nmax; ++hs) {
+        if (hs > 0) {
+          const TileRow tmp = ta;
+          ta = tb;
+          tb = tmp;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pfull(x));
+        softmax_tile(ta, tb, hs & 1, hs >> 1);
+      }
+      if (nmax > 0) {  // the last half-step was Q tile 1
+        tr[0] = tb;
+        tr[1] = ta;
+      }
+    } else {
+      for (int j = 0; j < nmax; ++j) {
+        softmax_tile(tr[0], tr[1], 0, j);
+        softmax_tile(tr[1], tr[0], 1, j);
       }
     }
 #pragma unroll
