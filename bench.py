@@ -200,10 +200,34 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def _strip_comments(src: str) -> str:
+    """C++ source without comments and trailing blanks: edits to comments leave the hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            e = src.find("*/", i + 2)
+            i = n if e < 0 else e + 2
+        elif src[i] == '"':  # string literal (inline PTX): copied as is
+            e = i + 1
+            while e < n and src[e] != '"':
+                e += 2 if src[e] == "\\" else 1
+            out.append(src[i:e + 1])
+            i = e + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the prefill kernel's sources, comments removed."""
     h = hashlib.sha256()
     for f in ("prefill.cu", "ptx.cuh", "tmem_wide.cuh", "internal.h"):
-        h.update(open(os.path.join(ROOT, "block_sparse_long_softmax_b300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "block_sparse_long_softmax_b300", "csrc", f)).read()
+        h.update(_strip_comments(src).encode())
     return h.hexdigest()[:16]
 
 

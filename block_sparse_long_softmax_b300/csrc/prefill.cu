@@ -13,18 +13,20 @@
 // CTA = 256 query rows of one (batch, query head) = two 128-row Q tiles.
 //   warp 0      TMA producer of Q (once) and the K_j ring
 //   warp 2      TMA producer of the V_j ring (decoupled from the K ring)
-//   warp 1      TMEM allocator and MMA issuer (one thread):
+//   warp 1      TMEM allocator and MMA issuer (the warp runs converged, one
+//               elected lane issues):
 //                 S_x = Q_x K_j^T   (A, B from shared memory, D in TMEM)
 //                 O_x += P_x V_j    (A = P from TMEM, B = V from shared memory)
 //   warp 3      idle
 //   warps 4-7   softmax of both Q tiles, in the order (x=0, j), (x=1, j),
 //                 (x=0, j+1), ...: one thread per row = one TMEM lane; the whole
-//                 S row is read into registers at once, the row max votes, and
+//                 S row is read into registers by one reduced load that also
+//                 returns the row max (tcgen05.ld.red), the row max votes, and
 //                 for kept tiles bf16 P is written over S in TMEM
 // While the softmax warps work on one Q tile the tensor core runs P.V and the
 // next Q.K^T of the other.  Each SMSP hosts one softmax warp: a second one would
-// take the issue slots the MMA-issuing thread needs (measured: the tensor core
-// slows by a third when two exp-heavy warps share the issuing thread's SMSP).
+// take the issue slots the MMA-issuing warp needs (measured: the tensor core
+// slows by a third when two exp-heavy warps share the issuing warp's SMSP).
 // The running max used by the vote is always the exact prefix max; the
 // accumulator's reference max is only moved when the max has grown by more
 // than 2^8 (lazy rescaling), which changes no result.

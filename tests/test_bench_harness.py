@@ -92,3 +92,13 @@ def test_reference_arm_prints_one_oracle_line(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert "9 splits" in line["config"]["sample_per_step"]
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    src = 'int f() { // a\n  return 1; /* b */ }\nconst char* s = "// kept";\n'
+    same = 'int f() { // another\n  return 1; /* c\n d */ }\nconst char* s = "// kept";\n'
+    other = 'int f() { // a\n  return 2; /* b */ }\nconst char* s = "// kept";\n'
+    strip = bench._strip_comments
+    assert strip(src) == strip(same)
+    assert strip(src) != strip(other)
+    assert '"// kept"' in strip(src)
