@@ -1,5 +1,6 @@
 // C ABI of libskipsm: argument validation, tensor maps, launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -104,15 +105,19 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 int* device_status_word() {
-  static int* ptrs[64] = {nullptr};
+  // one slot per device; host threads may race on the first lookup, and all of them
+  // store the same address
+  static std::atomic<int*> ptrs[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
+  int* w = ptrs[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
+    w = static_cast<int*>(p);
+    ptrs[dev].store(w, std::memory_order_release);
   }
-  return ptrs[dev];
+  return w;
 }
 
 }  // namespace skipsm
