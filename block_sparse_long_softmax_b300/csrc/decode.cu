@@ -396,17 +396,19 @@ cudaError_t launch_split(const CUtensorMap& kmap, const CUtensorMap& vmap, const
 }  // namespace
 
 size_t decode_smem_bytes(const DecodeParams& p) {
-  return p.D == 128 ? split_smem<128, 3, 2, 2>(p) : split_smem<64, 6, 3, 1>(p);
+  return p.D == 128 ? split_smem<128, 3, 2, 2>(p) : split_smem<64, 6, 3, 2>(p);
 }
 
-// D = 128: three key tiles in flight and P.V two tiles behind the vote (LAG = 2), so a kept
-// tile's value fetch, which can only start once the tile is voted on, has two tiles of key
-// streaming to land in.  Against four key tiles and LAG = 1 this measured 4-8 % faster at
-// skip ratios 0.24-0.81 and no slower at lambda = 0 (128K: 613 against 618 us).
+// P.V runs two tiles behind the vote (LAG = 2), so a kept tile's value fetch, which can only
+// start once the tile is voted on, has two tiles of key streaming to land in.  D = 128 keeps
+// three key tiles in flight: against four key tiles and LAG = 1 this measured 4-8 % faster at
+// skip ratios 0.24-0.81 and no slower at lambda = 0 (128K: 613 against 618 us).  D = 64 keeps
+// six: against LAG = 1, 3-6 % faster at every measured skip ratio (128K: 399 against 423 us at
+// lambda = 0).
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
                           int B, cudaStream_t stream) {
   if (p.D == 128) return launch_split<128, 3, 2, 2>(kmap, vmap, p, B, stream);
-  return launch_split<64, 6, 3, 1>(kmap, vmap, p, B, stream);
+  return launch_split<64, 6, 3, 2>(kmap, vmap, p, B, stream);
 }
 
 cudaError_t launch_combine(const CombineParams& p, int B, cudaStream_t stream) {
