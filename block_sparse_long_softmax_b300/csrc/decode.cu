@@ -393,6 +393,11 @@ cudaError_t launch_split(const CUtensorMap& kmap, const CUtensorMap& vmap, const
   return cudaGetLastError();
 }
 
+// The default split count assumes two split CTAs resident per SM (228 KB of shared memory
+// per SM, 1 KB of it reserved per CTA); both configurations below must keep that.
+static_assert(2 * (DecodeCfg<128, 3, 2, 2>::kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(2 * (DecodeCfg<64, 6, 3, 2>::kAlloc + 1024) <= 228 * 1024, "two CTAs per SM");
+
 }  // namespace
 
 size_t decode_smem_bytes(const DecodeParams& p) {
