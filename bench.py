@@ -40,7 +40,33 @@ PREFILL = "prefill_128k_gqa8"
 DECODE = "decode_128k_gqa8"
 TARGET_RHO = 0.5
 SWEEP_RHO = (0.3, 0.5, 0.7)
+DECODE_SWEEP_RHO = (0.3, 0.5, 0.7, 0.8)
 L2_BYTES = 126 * 2**20
+# The step's thresholds: the values the library's calibration (bisection on log10 lambda
+# over the kernels' own skip counts) returns for a 50% tile skip ratio on these two
+# workloads, rounded to four digits.  Both arms take them, so their configs are the same;
+# the line reports the skip ratio each one gives.
+PREFILL_LAMBDA = 3.045e-3
+DECODE_LAMBDA = 1.251e-3
+# Splits the library's default model picks for the 128K decode (B=8, Hkv=8) on 148 SMs;
+# the reference arm takes it as an argument so that it needs no library.
+DECODE_SPLITS = 9
+# Rows whose outputs are compared with the oracle's dense attention in the sweep:
+# prefill (b=0, head 5), the first, middle and last 128-row query tiles; decode
+# groups (b=0, kv head 0) and (b=7, kv head 7).
+ERR_PREFILL_HEAD = 5
+ERR_PREFILL_QTILES = (0, 511, 1023)
+ERR_DECODE_GROUPS = ((0, 0), (7, 7))
+
+
+def workload_config(lam_pf: float, lam_dec: float, splits: int, ws: int) -> dict:
+    """The `config` object of the JSON line (the same in both arms)."""
+    return {
+        "workload": "prefill 128K causal (B=1, Hq=64, Hkv=8, D=128, 128x128 tiles) + "
+                    "decode 128K (B=8, Hq=64, Hkv=8, D=128, 64-key tiles)",
+        "prefill_lambda": lam_pf, "decode_lambda": lam_dec, "decode_splits": splits,
+        "l2": "inputs larger than L2 (Q 2.1 GB, K/V 268 MB each; decode K/V 2.1 GB each); "
+              "no flush", "parallelism": f"replicas x{ws} (independent problems)"}
 
 
 # ---------------------------------------------------------------------------
@@ -311,18 +337,43 @@ def oracle_sample(budget_s: float, lam_pf: float, lam_dec: float, splits: int, s
     return flops, sec, desc
 
 
+def oracle_dense_rows(wp, wd, splits):
+    """The oracle's dense attention (lambda = 0) on the rows the sweep checks:
+    ([rows][D] prefill, [groups][G][D] decode), fp64."""
+    import numpy as np
+    import oracle
+    import synth
+    from synth import planted as P
+
+    tp, td = synth.make_tables(wp), synth.make_tables(wd)
+    h = ERR_PREFILL_HEAD
+    qh = synth.bf16_bits_to_f64(P.gen_q_rows(wp, tp, 0, h))
+    kh = synth.bf16_bits_to_f64(P.gen_k_rows(wp, tp, 0, h // wp.G))
+    vh = synth.bf16_bits_to_f64(P.gen_v_rows(wp, 0, h // wp.G))
+    pf = np.concatenate([oracle.prefill_qtile(qh, kh, vh, t, tile_q=128, tile_k=128, causal=True,
+                                              lam=0.0, scale=1.0 / math.sqrt(wp.D))[0]
+                         for t in ERR_PREFILL_QTILES])
+    dec = []
+    for b, hk in ERR_DECODE_GROUPS:
+        qg = synth.bf16_bits_to_f64(np.stack([P.gen_q_rows(wd, td, b, hq)[0]
+                                              for hq in range(hk * wd.G, (hk + 1) * wd.G)]))
+        kd = synth.bf16_bits_to_f64(P.gen_k_rows(wd, td, b, hk))
+        vd = synth.bf16_bits_to_f64(P.gen_v_rows(wd, b, hk))
+        dec.append(oracle.decode_group(qg, kd, vd, lam=0.0, num_splits=splits, tile_k=64)[0])
+    return pf, np.stack(dec)
+
+
 def run_reference(args):
+    """The oracle alone, on the host cores, at the thresholds and split count of our arm
+    (passed as arguments: the oracle cannot calibrate, and this arm loads no library)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     total_f, total_s = 0.0, 0.0
     desc = ""
-    import block_sparse_long_softmax_b300 as bs  # host-only query: the split geometry
-    import synth
-    wd = synth.WORKLOADS[DECODE]
-    splits = bs.decode_num_splits(wd.B, wd.Hkv, wd.Skv, 0)  # the same split geometry as ours
     for i in range(args.warmup + args.steps):
-        f, s, desc = oracle_sample(args.ref_budget, 1e-3, 1e-3, splits, seed_off=i % 3)
+        f, s, desc = oracle_sample(args.ref_budget, args.ref_prefill_lambda,
+                                   args.ref_decode_lambda, args.ref_splits, seed_off=i % 3)
         if i >= args.warmup:
             total_f += f
             total_s += s
@@ -333,8 +384,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic planted-structure (seeded), bounded sample per step",
-        "config": {"workload": "prefill 128K causal Hq=64 Hkv=8 D=128 + decode 128K B=8",
-                   "sample_per_step": desc},
+        "config": workload_config(args.ref_prefill_lambda, args.ref_decode_lambda,
+                                  args.ref_splits, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -392,9 +443,14 @@ def run_ours(args):
         run_decode(lam)
         return int(cntd[:: wd.G].sum().item()) / nblk_d
 
-    # lambda for each target skip ratio, found by the library's calibration (bisection)
+    # lambda for each target skip ratio, found by the library's calibration (bisection);
+    # the timed step uses the fixed thresholds both arms share
     lam_pf = {r: bs.calibrate_prefill(q, k, v, r, out=o)[0] for r in SWEEP_RHO}
-    lam_dec = bs.calibrate_decode(qd, kd, vd, TARGET_RHO, workspace=wsp, out=od)[0]
+    lam_dec_rho = {r: bs.calibrate_decode(qd, kd, vd, r, workspace=wsp, out=od)[0]
+                   for r in DECODE_SWEEP_RHO}
+    lam_step, lam_dec = PREFILL_LAMBDA, DECODE_LAMBDA
+    err_rows = [r for t in ERR_PREFILL_QTILES for r in range(128 * t, 128 * t + 128)]
+    err_gpu_pf, err_gpu_dec = [], []   # sampled GPU rows per sweep entry (for the oracle check)
 
     def time_events(fn, reps):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -411,11 +467,12 @@ def run_ours(args):
     # ---- lambda sweeps (device time, inputs resident)
     o_ref = None
     sweep_pf = []
-    lams = [0.0] + [lam_pf[r] for r in SWEEP_RHO] + [1e-4, 1e-3, 1e-2]
+    lams = [0.0] + [lam_pf[r] for r in SWEEP_RHO] + [lam_step, 1e-4, 1e-3, 1e-2]
     t_dense = None
     for lam in lams:
         sec = time_events(lambda: run_prefill(lam), 3)
         rho = prefill_rho(lam)
+        err_gpu_pf.append(o[0, ERR_PREFILL_HEAD, err_rows].float().cpu())
         if lam == 0.0:
             o_ref = o.clone()
             t_dense = sec
@@ -432,7 +489,7 @@ def run_ours(args):
             "mean_abs_err_vs_lambda0": err_mean})
     # Rowmax-PoT weights on the kept tiles (same skip decisions), against the exact lambda=0 output
     sweep_pot = []
-    for lam in (0.0, lam_pf[TARGET_RHO]):
+    for lam in (0.0, lam_step):
         def run_pot():
             bs.prefill(q, k, v, lam, causal=True, out=o, skip_counts=cnt, exp_mode="pot")
         sec = time_events(run_pot, 3)
@@ -447,7 +504,7 @@ def run_ours(args):
     # FP8/BF16 mixed precision: e4m3 Q and K (the same inputs rounded), bf16 V
     q8, k8 = q.to(torch.float8_e4m3fn), k.to(torch.float8_e4m3fn)
     sweep_fp8 = []
-    for lam in (0.0, lam_pf[TARGET_RHO]):
+    for lam in (0.0, lam_step):
         def run_fp8():
             bs.prefill(q8, k8, v, lam, causal=True, out=o, skip_counts=cnt)
         sec = time_events(run_fp8, 3)
@@ -473,7 +530,7 @@ def run_ours(args):
     causal_pairs = wp.B * wp.Hq * nqt_m * (nqt_m + 1) // 2
     sel_pairs = int(torch.tril(pm.to(torch.int64)).sum().item())
     sweep_pbm = []
-    for lam in (0.0, lam_pf[TARGET_RHO]):
+    for lam in (0.0, lam_step):
         def run_pbm():
             bs.prefill(q, k, v, lam, causal=True, out=o, skip_counts=cnt, block_mask=pm)
         sec = time_events(run_pbm, 3)
@@ -487,9 +544,11 @@ def run_ours(args):
     od_ref = None
     sweep_dec = []
     t_dense_d = None
-    for lam in [0.0, 1e-4, 1e-3, 1e-2, lam_dec]:
+    for lam in [0.0, 1e-4, 1e-3, 1e-2, lam_dec] + [lam_dec_rho[r] for r in DECODE_SWEEP_RHO]:
         sec = time_events(lambda: run_decode(lam), 20)
         rho = decode_rho(lam)
+        err_gpu_dec.append(torch.stack([od[b, hk * wd.G:(hk + 1) * wd.G].float().cpu()
+                                        for b, hk in ERR_DECODE_GROUPS]))
         kept = nblk_d - int(cntd[:: wd.G].sum().item())
         if lam == 0.0:
             od_ref = od.clone()
@@ -544,7 +603,6 @@ def run_ours(args):
     del selm
 
     # ---- the timed steps
-    lam_step = lam_pf[TARGET_RHO]
     ev_pf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps)]
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -667,13 +725,22 @@ def run_ours(args):
     peaks, src = measured_peaks()
     exec_flops = prefill_exec_flops(wp, visited, skipped_pf, 128, 128)
     achieved = exec_flops / t_pf / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(PREFILL),
+    burst = peaks.get("bf16_tflops")
+    sustained = peaks.get("bf16_tflops_sustained")
+    smax = peaks.get("sm_max_mhz") or 2032.0
+    mhz = clocks.get("sm_mhz")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                "frac": achieved / burst, "traffic": profiled_traffic(PREFILL),
                 "kernel": "prefill_kernel<128,128,128,3,2,0,0,0>",
-                "peak_source": f"{src} bf16_tflops_sustained (cuBLAS, power-capped loop)",
-                "burst_peak": peaks.get("bf16_tflops"),
-                "frac_of_burst": achieved / peaks.get("bf16_tflops", peak),
+                "peak_source": f"{src} bf16_tflops (cuBLAS 8192^3, best of 10: burst)",
+                # the same peak scaled to the clock this kernel ran at (median SM MHz of the
+                # timed region), taking the burst GEMM to have run at the maximum SM clock
+                "frac_clock_normalised": (achieved / (burst * mhz / smax)) if mhz else None,
+                "kernel_sm_mhz": mhz,
+                "sustained_peak": sustained,
+                "frac_of_sustained": achieved / sustained if sustained else None,
+                "sustained_note": "cuBLAS in a 4 s power-capped loop at a median "
+                                  f"{peaks.get('clocks_under_load', {}).get('sm_mhz_median')} MHz",
                 "algorithmic_flops_per_launch": exec_flops}
 
     line = {
@@ -681,13 +748,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
         "data": "synthetic planted-structure inputs generated on the GPU (seeded), no weights",
-        "config": {
-            "workload": "prefill 128K causal (B=1, Hq=64, Hkv=8, D=128, 128x128 tiles) + "
-                        "decode 128K (B=8, Hq=64, Hkv=8, D=128, 64-key tiles)",
-            "prefill_lambda": lam_step, "prefill_skip_ratio": rho_pf,
-            "decode_lambda": lam_dec, "decode_skip_ratio": rho_dec, "decode_splits": nsplit,
-            "l2": "inputs larger than L2 (Q 2.1 GB, K/V 268 MB each; decode K/V 2.1 GB each); "
-                  "no flush", "parallelism": f"replicas x{ws} (independent problems)"},
+        "config": workload_config(lam_step, lam_dec, nsplit, ws),
         "prefill": {"ms": t_pf * 1e3, "dense_equiv_tflops": prefill_dense_flops(wp) / t_pf / 1e12,
                     "executed_tflops": achieved, "skip_ratio": rho_pf, "lambda": lam_step},
         "decode": {"us_per_step": t_dec * 1e6,
@@ -710,6 +771,20 @@ def run_ours(args):
         f, s, desc = oracle_sample(args.cpu_budget, lam_step, lam_dec, nsplit)
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": UNIT, "cores": blas_threads(),
                                 "kind": "oracle", "sample": desc, "seconds": s}
+        # the same leg evaluates the oracle's dense attention (lambda = 0) on the sampled
+        # rows, and the sweep entries get their error against it
+        dense_pf, dense_dec = oracle_dense_rows(wp, wd, nsplit)
+        for ent, g in zip(sweep_pf, err_gpu_pf):
+            d = (g.double().numpy() - dense_pf).__abs__()
+            ent["max_abs_err_vs_oracle_dense"] = float(d.max())
+            ent["mean_abs_err_vs_oracle_dense"] = float(d.mean())
+        for ent, g in zip(sweep_dec, err_gpu_dec):
+            d = (g.double().numpy() - dense_dec).__abs__()
+            ent["max_abs_err_vs_oracle_dense"] = float(d.max())
+            ent["mean_abs_err_vs_oracle_dense"] = float(d.mean())
+        line["sweep"]["oracle_dense_rows"] = (
+            f"prefill b=0 head {ERR_PREFILL_HEAD} query tiles {list(ERR_PREFILL_QTILES)} "
+            f"(128 rows each); decode groups (b, kv head) {list(ERR_DECODE_GROUPS)}")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg_on:
@@ -805,6 +880,13 @@ def main(argv=None):
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=4.0,
                     help="seconds of oracle work per reference step")
+    ap.add_argument("--ref-prefill-lambda", type=float, default=PREFILL_LAMBDA,
+                    help="prefill threshold of the reference arm (our arm's step value)")
+    ap.add_argument("--ref-decode-lambda", type=float, default=DECODE_LAMBDA,
+                    help="decode threshold of the reference arm (our arm's step value)")
+    ap.add_argument("--ref-splits", type=int, default=DECODE_SPLITS,
+                    help="decode splits of the reference arm (the library's default for the "
+                         "128K decode on 148 SMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the raw nvidia-smi samples of the timed region "

@@ -38,7 +38,8 @@ class PrefillOpts(ctypes.Structure):
                 ("skip_mask", ctypes.c_void_p), ("visited_counts", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int),
                 ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float),
-                ("block_mask", ctypes.c_void_p), ("inject_wait_timeout", ctypes.c_int)]
+                ("block_mask", ctypes.c_void_p), ("inject_wait_timeout", ctypes.c_int),
+                ("status", ctypes.c_void_p)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
@@ -54,7 +55,7 @@ class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("lse", ctypes.c_void_p), ("skip_mask", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("inject_wait_timeout", ctypes.c_int),
-                ("block_mask", ctypes.c_void_p)]
+                ("block_mask", ctypes.c_void_p), ("status", ctypes.c_void_p)]
 
 
 class Calibration(ctypes.Structure):
@@ -126,6 +127,17 @@ def _check_tensor(name, t, ndim, fp8=False):
         raise TypeError(f"{name} must be a contiguous {want} tensor with {ndim} dims")
 
 
+def _status_ptr(status):
+    """Device address of a caller's per-call status word (None = the shared word)."""
+    import torch
+    if status is None:
+        return None
+    if (not isinstance(status, torch.Tensor) or not status.is_cuda or status.dtype != torch.int32
+            or status.numel() != 1):
+        raise TypeError("status must be a one-element int32 CUDA tensor")
+    return status.data_ptr()
+
+
 def check(stream=None) -> int:
     """Synchronise `stream`, read and clear the device status word (0 = clean)."""
     st = ctypes.c_int(0)
@@ -151,13 +163,15 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
             wait_limit_ms: int = 0, exp_mode: str = "exact",
             qk_descale: float = 0.0, block_mask=None,
-            inject_wait_timeout: bool = False) -> PrefillOut:
+            inject_wait_timeout: bool = False, status=None) -> PrefillOut:
     """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
     q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
     Q.K^T in e4m3, scaled by qk_descale); v is bf16.  exp_mode "exact" uses exponentials on
     kept tiles, "pot" Rowmax-PoT powers of two.  block_mask: optional uint8/bool CUDA
     tensor [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)] of the pairs to visit.
+    status: optional int32 CUDA tensor of one element that receives this call's
+    device status (a timed-out wait's site) instead of the library's shared word.
     """
     import torch
     lib = library()
@@ -183,7 +197,7 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
                        ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
                        float(qk_descale), ptr(block_mask).value,
-                       1 if inject_wait_timeout else 0)
+                       1 if inject_wait_timeout else 0, _status_ptr(status))
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))
@@ -210,11 +224,11 @@ class DecodeOut:
 def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0.0,
            return_lse: bool = False, return_mask: bool = False, workspace=None, out=None,
            skip_counts=None, stream=None, wait_limit_ms: int = 0,
-           inject_wait_timeout: bool = False, block_mask=None) -> DecodeOut:
+           inject_wait_timeout: bool = False, block_mask=None, status=None) -> DecodeOut:
     """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors.
 
     block_mask: optional uint8/bool CUDA tensor [B][Hkv][ceil(Skv/64)] of the key tiles
-    to visit (nonzero = visit).
+    to visit (nonzero = visit).  status: as for prefill.
     """
     import torch
     lib = library()
@@ -237,7 +251,8 @@ def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0
             raise TypeError(f"block_mask must be a contiguous uint8/bool CUDA tensor "
                             f"of shape {(B, Hkv, nblk)}")
     opts = DecodeOpts(int(num_splits), float(softmax_scale), ptr(lse).value, ptr(mask).value,
-                      int(wait_limit_ms), 1 if inject_wait_timeout else 0, ptr(block_mask).value)
+                      int(wait_limit_ms), 1 if inject_wait_timeout else 0, ptr(block_mask).value,
+                      _status_ptr(status))
     _raise(lib.skipsm_decode_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Skv, D, float(lam),
                                 ptr(cnt), ptr(ws), ws.numel() * ws.element_size(),
                                 ctypes.byref(opts), _P(_stream(stream))))

@@ -15,6 +15,13 @@ namespace skipsm {
 
 __device__ int g_device_status = 0;
 
+#if SKIPSM_TRACE
+// Test-only instrumentation: the next prefill launches stamp the events of CTA
+// `g_trace_cta` into `g_trace_buf` (see skipsm_debug_prefill_trace).
+unsigned long long* g_trace_buf = nullptr;
+int g_trace_cta = -1;
+#endif
+
 namespace {
 
 thread_local char t_last_error[512] = "";
@@ -91,33 +98,78 @@ void set_lambda(float lambda, float* lam_log2, int* lam_pos) {
 }
 
 constexpr int kDecodeBk = 64;
-// Default split count: split CTAs run in waves of kDecodeSms * kDecodeCtasPerSm (two
+// Default split count: split CTAs run in waves of (SMs) * kDecodeCtasPerSm (two
 // resident per SM at D = 128, bound by shared memory), and a wave that is only partly
 // filled costs nearly as much as a full one.  Each CTA also pays a start-up of about
-// kDecodeCtaStartTiles tile loads before its pipeline is full.
+// kDecodeCtaStartTiles tile loads before its pipeline is full.  The SM count is read
+// from the device; kDecodeSms (B300) stands in when no device can be queried.
 constexpr int kDecodeSms = 148;
 constexpr int kDecodeCtasPerSm = 2;
 constexpr int kDecodeCtaStartTiles = 4;
-constexpr int kDecodeMaxDefaultSplits = kDecodeSms * kDecodeCtasPerSm * 8;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int device_sm_count() {
+  static std::atomic<int> counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();  // no device here: clear the error, use the B300 count
+    return kDecodeSms;
+  }
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return kDecodeSms;
+    }
+    counts[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 int* device_status_word() {
-  // one slot per device; host threads may race on the first lookup, and all of them
-  // store the same address
-  static std::atomic<int*> ptrs[64] = {};
+  // One slot per device, keyed by the context it was looked up in: a device reset or
+  // another context on the device gets its own lookup.
+  struct Slot { unsigned long long ctx; int* ptr; };
+  static std::mutex mu;
+  static Slot slots[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  int* w = ptrs[dev].load(std::memory_order_acquire);
-  if (!w) {
+  std::lock_guard<std::mutex> lock(mu);
+  unsigned long long ctx = current_context_id();
+  if (!slots[dev].ptr || ctx == 0 || slots[dev].ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    w = static_cast<int*>(p);
-    ptrs[dev].store(w, std::memory_order_release);
+    // the lookup made the device's primary context current if none was
+    if (ctx == 0) ctx = current_context_id();
+    slots[dev] = Slot{ctx, static_cast<int*>(p)};
   }
-  return w;
+  return slots[dev].ptr;
 }
 
 }  // namespace skipsm
@@ -127,6 +179,16 @@ using namespace skipsm;
 extern "C" {
 
 int skipsm_version(void) { return SKIPSM_VERSION; }
+
+#if SKIPSM_TRACE
+// Only in SKIPSM_TRACE builds (libskipsm_trace.so): later prefill calls record clock64
+// stamps of CTA `cta` into `buf` (device, [key tiles][2][16] uint64, zeroed by the
+// caller); buf = NULL stops recording.  Not part of the library's interface.
+void skipsm_debug_prefill_trace(void* buf, int cta) {
+  g_trace_buf = static_cast<unsigned long long*>(buf);
+  g_trace_cta = cta;
+}
+#endif
 
 const char* skipsm_last_error(void) { return t_last_error; }
 
@@ -183,8 +245,10 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
     return fail(SKIPSM_ERR_INVALID_ARG, "qk_descale must be finite and >= 0");
   const long long nblk_q = (Sq + 255) / 256;
   if (nblk_q * B * Hq > 0x7FFFFFFFLL) return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
-  int* status = device_status_word();
+  int* status = op.status ? op.status : device_status_word();
   if (!status) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
+  if (reinterpret_cast<uintptr_t>(status) & 3u)
+    return fail(SKIPSM_ERR_INVALID_ARG, "status must be 4-byte aligned");
 
   CUtensorMap qmap, kmap, vmap;
   const int qk_elem = op.qk_format == 1 ? 1 : 2;
@@ -215,6 +279,10 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.wait_cycles = wait_cycles(op.wait_limit_ms);
   p.exp_mode = op.exp_mode;
   p.inject_fault = op.inject_wait_timeout ? 1 : 0;
+#if SKIPSM_TRACE
+  p.trace = g_trace_buf;
+  p.trace_cta = g_trace_cta;
+#endif
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -248,8 +316,8 @@ int skipsm_decode_num_splits(int B, int Hkv, int Skv, int requested) {
     // the large logits of earlier keys keeps tiles a longer prefix would skip.  Splits
     // hold at least 16 tiles.
     const long long items = static_cast<long long>(B) * Hkv;
-    const long long slots = static_cast<long long>(kDecodeSms) * kDecodeCtasPerSm;
-    const int hi = std::min(std::max(1, nblk / 16), kDecodeMaxDefaultSplits);
+    const long long slots = static_cast<long long>(device_sm_count()) * kDecodeCtasPerSm;
+    const int hi = static_cast<int>(std::min<long long>(std::max(1, nblk / 16), slots * 8));
     long long best = -1;
     want = 1;
     for (int s = 1; s <= hi; ++s) {
@@ -307,8 +375,10 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
                 workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(SKIPSM_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  int* status = device_status_word();
+  int* status = op.status ? op.status : device_status_word();
   if (!status) return fail(SKIPSM_ERR_CUDA, "device status word unavailable");
+  if (reinterpret_cast<uintptr_t>(status) & 3u)
+    return fail(SKIPSM_ERR_INVALID_ARG, "status must be 4-byte aligned");
 
   CUtensorMap kmap, vmap;
   if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, kDecodeBk))) return st;

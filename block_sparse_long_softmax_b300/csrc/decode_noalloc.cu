@@ -20,7 +20,10 @@
 //     by the split step of the same call.
 //   * The first call on each device looks up the array's device address (one
 //     cudaGetSymbolAddress with that device current).  Make that first call
-//     before starting any stream capture on the device.
+//     before starting any stream capture on the device.  The address is kept
+//     with the id of the context it belongs to; a call from another context
+//     (or after a device reset recreated the primary context) looks it up again,
+//     so such a call, too, must come before any capture.
 #include <cstring>
 #include <mutex>
 
@@ -36,22 +39,31 @@ static_assert(kScratchBytes % 256 == 0, "scratch size keeps 256-byte alignment")
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 std::mutex g_lookup_mu;
-void* g_scratch_ptr[64] = {nullptr};
+struct ScratchSlot {
+  unsigned long long ctx;  // id of the context the address belongs to
+  void* ptr;
+};
+ScratchSlot g_scratch[64] = {};
 
-// Device address of g_decode_scratch on the current device (looked up once).
+// Device address of g_decode_scratch in the context current on this thread.  It is
+// looked up once per device (cudaGetSymbolAddress with that device current) and again
+// only if the current context is not the one it was looked up in (a device reset
+// that recreated the primary context, or another context made current).
 skipsm_status scratch_on_current_device(void** out, int* dev_out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return SKIPSM_ERR_CUDA;
   if (dev < 0 || dev >= 64) return SKIPSM_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_lookup_mu);
-  if (!g_scratch_ptr[dev]) {
+  unsigned long long ctx = skipsm::current_context_id();
+  if (!g_scratch[dev].ptr || ctx == 0 || g_scratch[dev].ctx != ctx) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
     if (e != cudaSuccess || ptr == nullptr) return SKIPSM_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    if (ctx == 0) ctx = skipsm::current_context_id();
+    g_scratch[dev] = ScratchSlot{ctx, ptr};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   *dev_out = dev;
   return SKIPSM_OK;
 }

@@ -82,6 +82,12 @@ struct PrefillParams {
   uint8_t* skip_mask;    // [B][Hq][nqt][nkt] or null
   int* status;
   long long wait_cycles;
+#if SKIPSM_TRACE
+  // test-only instrumentation (SKIPSM_TRACE builds): clock64 stamps of one CTA,
+  // [key tile][Q tile][16] per-tile events of the softmax and MMA warps
+  unsigned long long* trace;
+  int trace_cta;
+#endif
 };
 
 cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -89,5 +95,15 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
                            cudaStream_t stream);
 
 int* device_status_word();  // library-global device status word
+
+// Unique id of the CUDA context current on this thread (cuCtxGetId), or 0 when no
+// context is current or the driver entry points are unavailable.  Addresses of
+// the library's __device__ arrays are cached per device together with this id and
+// looked up again when it changes (another context, or a device reset that
+// recreated the primary context).
+unsigned long long current_context_id();
+
+// Multiprocessors of the current device (148 on B300; 148 when it cannot be queried).
+int device_sm_count();
 
 }  // namespace skipsm

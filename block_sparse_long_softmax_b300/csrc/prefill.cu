@@ -41,6 +41,19 @@ constexpr int kThreads = 256;
 constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
 constexpr float kRescaleLog2 = 8.f;
 
+// Test-only instrumentation (built with -DSKIPSM_TRACE=1 into a separate library):
+// one lane of the softmax warp of TMEM quadrant 0 and of the MMA warp stamp clock64
+// at fixed points of each (key tile j, Q tile x) into p.trace[(j * 2 + x) * 16 + e].
+// Events: 0 softmax entry, 1 S ready, 2 row max loaded, 3 vote decided, 4 P stored,
+// 5 P arrived; 6 = 1 if the CTA kept the tile (a flag, not a time); 8 MMA warp waits
+// for P, 9 P seen, 10 P.V issued, 11 next Q.K^T issued and committed.
+#if SKIPSM_TRACE
+#define SKIPSM_STAMP(on, j, x, e, val) \
+  do { if (on) p.trace[((j) * 2 + (x)) * 16 + (e)] = (val); } while (0)
+#else
+#define SKIPSM_STAMP(on, j, x, e, val) do { } while (0)
+#endif
+
 template <int D, int BK, int TQ, int NK, int NV, bool F8>
 struct PrefillCfg {
   // Q and K are bf16, or e4m3 with F8; V is always bf16.  Operand rows are cut into
@@ -275,6 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         umma_commit_w(kempty(0), issue);
       }
+#if SKIPSM_TRACE
+      const bool tr_on = p.trace && static_cast<int>(blockIdx.x) == p.trace_cta && lane == 0;
+#else
+      const bool tr_on = false;
+#endif
       for (int j = 0; ok && j < nmax; ++j) {
         const int vs = j % NV, ks1 = (j + 1) % NK;
         const bool has_next = j + 1 < nmax;
@@ -295,8 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= nx[x]) continue;
+          SKIPSM_STAMP(tr_on, j, x, 8, clock64());
           if (!wait(pfull(x), j & 1, kSitePrefillPFull)) { ok = false; break; }
           tc_fence_after();
+          SKIPSM_STAMP(tr_on, j, x, 9, clock64());
           if (sdec[x]) {
             if (!v_ready) {
               if (!wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) { ok = false; break; }
@@ -305,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issue_pv(x, vs);
           }
+          SKIPSM_STAMP(tr_on, j, x, 10, clock64());
           if (j + 1 < nx[x]) {
             if (!k_ready) {  // K_{j+1} is first needed here, after P.V of tile j is queued
               if (!wait(kfull(ks1), ((j + 1) / NK) & 1, kSitePrefillKFull)) { ok = false; break; }
@@ -313,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issue_s(x, ks1);
             umma_commit_w(sfull(x), issue);
+            SKIPSM_STAMP(tr_on, j, x, 11, clock64());
           } else {
             // the last tile of this Q tile: one commit lets the epilogue wait for its final P.V
             umma_commit_w(odone(x), issue);
@@ -376,6 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WaitCtx half{p.wait_cycles / 2, p.status, abort_flag};
       ok = mbar_wait(never_bar, 0, half, kSitePrefillInjected);
     }
+#if SKIPSM_TRACE
+    const bool tr_on = p.trace && static_cast<int>(blockIdx.x) == p.trace_cta && r == 0;
+#else
+    const bool tr_on = false;
+#endif
     bool next_ready = false;  // the S of the next tile in this order is known to be complete
     // The softmax of one (Q tile x, key tile j): t is the row state of Q tile x, o that of the
     // other Q tile.
@@ -391,11 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t tS = lane_base + (x == 0 ? C::kColS0 : C::kColS1);
       const uint32_t tO = lane_base + (x == 0 ? C::kColO0 : C::kColO1);
+      SKIPSM_STAMP(tr_on, j, x, 0, clock64());
       if (!next_ready) ok = mbar_wait(sfull(x), j & 1, wc, kSitePrefillSFull) && ok;
       tc_fence_after();
+      SKIPSM_STAMP(tr_on, j, x, 1, clock64());
       uint32_t sv[BK];
       // the load also returns the row's maximum over the tile (tcgen05.ld.red)
       float mx = tmem_ld_max<BK>(tS, sv);
+      SKIPSM_STAMP(tr_on, j, x, 2, clock64());
       const int key0 = j * BK;
       // tile-level (warp-uniform) test: does any row of this warp see a masked key?
       if (j >= t.j_mask) {
@@ -465,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool any_kept = !(skip_g[0] && skip_g[1]);
       const bool my_skip = grp == 0 ? skip_g[0] : skip_g[1];
+      SKIPSM_STAMP(tr_on, j, x, 3, clock64());
+      SKIPSM_STAMP(tr_on, j, x, 6, any_kept ? 1ull : 0ull);
       bool counted = r == grp * TQ && j < t.n_grp;  // one thread per vote group records it
       if constexpr (BM) counted = counted && (grp == 0 ? sel0 : sel1);
       if (counted) {
@@ -554,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st<BK / 2>(tS, z);
         }
       }
+      SKIPSM_STAMP(tr_on, j, x, 4, clock64());
       {
         // Probe the next tile's S without blocking; its latency overlaps the
         // fence and arrive below, and a complete phase skips the wait.
@@ -564,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(pfull(x));
+      SKIPSM_STAMP(tr_on, j, x, 5, clock64());
     };
     if constexpr (POT) {
       // One copy of the longer Rowmax-PoT body serves both Q tiles (x at run time, the row

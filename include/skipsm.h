@@ -28,7 +28,12 @@
  *    before any launch and return SKIPSM_ERR_INVALID_ARG / _UNSUPPORTED with
  *    nothing enqueued; skipsm_last_error() gives the reason (thread-local).
  *  - Device-side failures (a pipeline wait that exceeded its bound) set a
- *    device status word instead of trapping; skipsm_check() reads and clears it.
+ *    device status word instead of trapping.  By default that is the library's
+ *    one word per device (per CUDA context), shared by every stream and host
+ *    thread: skipsm_check() reads and clears it for all of them, so with calls
+ *    from several streams or threads a failure may be reported to, and cleared
+ *    by, a caller other than the one whose launch timed out.  Such callers pass
+ *    their own word in the `status` option of the _ex calls instead.
  *  - Softmax scale is 1/sqrt(D) unless an _ex call gives one.  Causal masking
  *    is bottom-right aligned: query i sits at key position Skv - Sq + i.
  *  - lambda must be finite and in [0, 1].
@@ -48,7 +53,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 106
+#define SKIPSM_VERSION 107
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -66,7 +71,9 @@ int skipsm_version(void);
 const char* skipsm_last_error(void);
 
 /*
- * Waits for `stream`, then reads and clears the library's device status word.
+ * Waits for `stream`, then reads and clears the library's device status word
+ * (the one shared by every call on the current device that passed no `status`
+ * option; see the conventions above).
  * *device_status (if not NULL) receives the raw word: 0 = clean, otherwise a
  * code identifying the wait that timed out.  Returns SKIPSM_ERR_TIMEOUT when
  * the word was set, SKIPSM_ERR_CUDA when synchronisation failed.
@@ -115,6 +122,11 @@ typedef struct skipsm_prefill_opts {
                               wait on a barrier nothing arrives at (half of wait_limit_ms); the
                               kernel ends early, outputs are undefined and skipsm_check()
                               reports site 25 */
+  int* status;            /* optional device int, 4-byte aligned, owned by the caller: this
+                             call's kernels record a timed-out wait here (the site code, first
+                             writer wins) instead of in the library's shared word.  The call
+                             neither clears nor reads it: zero it before the call, read it after
+                             the stream has finished.  NULL = the shared word (skipsm_check) */
 } skipsm_prefill_opts;
 
 /*
@@ -145,7 +157,8 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
 
 /*
  * Number of KV splits a decode call uses when the caller asks for 0.  The
- * (b, kv head, split) CTAs run in waves of 2 per SM on the 148 SMs; the default
+ * (b, kv head, split) CTAs run in waves of 2 per SM (the current device's SM
+ * count; 148, the B300's, when no device can be queried); the default
  * is the count with the least modelled time, waves x (tiles per split + a
  * start-up of 4 tiles), taking the fewest splits on a tie and at least 16 key
  * tiles of 64 per split (every split keeps its first tile and restarts its
@@ -183,6 +196,7 @@ typedef struct skipsm_decode_opts {
                               lse = -inf.  NULL = every tile.  With a mask each split's tile
                               list is kept in shared memory (2 bytes per tile of the split);
                               SKIPSM_ERR_UNSUPPORTED if it does not fit. */
+  int* status;            /* optional per-call device status word, as in skipsm_prefill_opts */
 } skipsm_decode_opts;
 
 /*

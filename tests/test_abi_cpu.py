@@ -43,8 +43,18 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, f)
 
 
+def test_noalloc_scratch_fits_both_decode_workloads(lib):
+    # the allocation-free decode keeps its split partials in a fixed 16 MiB array; with the
+    # default split count both decode workloads (B=16 at 32K, B=8 at 128K; Hq=64, D=128) fit
+    import synth
+    for name in ("decode_32k_gqa8", "decode_128k_gqa8"):
+        w = synth.WORKLOADS[name]
+        need = lib.skipsm_decode_workspace_size(w.B, w.Hq, w.Hkv, w.Skv, w.D, 0)
+        assert 0 < need <= 16 << 20, (name, need)
+
+
 def test_version(lib):
-    assert lib.skipsm_version() == 106
+    assert lib.skipsm_version() == 107
 
 
 P = 0x10000  # a 16-byte aligned fake device address; validation never dereferences it

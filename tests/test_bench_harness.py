@@ -91,7 +91,24 @@ def test_reference_arm_prints_one_oracle_line(capsys):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
-    assert "9 splits" in line["config"]["sample_per_step"]
+    assert "9 splits" in line["cpu_baseline"]["sample"]
+    # the same config object as our arm's, at the step's thresholds and split count
+    assert line["config"] == bench.workload_config(bench.PREFILL_LAMBDA, bench.DECODE_LAMBDA,
+                                                   bench.DECODE_SPLITS, 1)
+
+
+def test_reference_arm_loads_no_library():
+    # the oracle arm is self-contained: it imports neither the package nor libskipsm.so
+    import subprocess
+    import sys
+    code = ("import sys, bench; bench.main(['--impl', 'reference', '--steps', '1', '--warmup', "
+            "'0', '--ref-budget', '0.01']); "
+            "assert 'block_sparse_long_softmax_b300' not in sys.modules, 'package imported'; "
+            "maps = open('/proc/self/maps').read(); assert 'libskipsm' not in maps, 'lib loaded'")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
 
 
 def test_kernel_source_hash_ignores_comments_only():

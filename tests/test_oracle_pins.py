@@ -45,6 +45,33 @@ def test_worked_prefill_noncausal():
     assert abs(r.o[0, 0, 0, 0] - want) < 1e-14
 
 
+def test_worked_skipped_mass():
+    # the non-causal example above at lambda = e^-0.5: key tile 1 (logits -10, 2) is skipped
+    # for both rows.  Dense probabilities are e^s / z with z = e^3 + e^0 + e^-10 + e^2, so the
+    # skipped mass is eps = (e^-10 + e^2) / z (about 0.2595) -- not 1 (all keys), not the kept
+    # mass, not a single key's probability.
+    q = np.array([[1.0], [1.0]])
+    k = np.array([[3.0], [0.0], [-10.0], [2.0]])
+    v = np.array([[1.0], [2.0], [3.0], [4.0]])
+    o_dense, lse, p = oracle.dense_attention(q, k, v, causal=False, scale=1.0)
+    skipped = np.array([[False, False, True, True]] * 2)
+    eps = oracle.skipped_mass(p, skipped)
+    z = E(3) + E(0) + E(-10) + E(2)
+    want = (E(-10) + E(2)) / z
+    assert np.allclose(eps, want, rtol=0, atol=1e-15)
+    assert abs(want - 0.25949) < 1e-4
+    assert abs(lse[0] - math.log(z)) < 1e-14
+    # the output moves by exactly eps times (skipped keys' mean value - kept output):
+    # o_dense = (1 - eps) o_kept + eps vbar_skipped
+    o_kept = (E(3) * 1 + E(0) * 2) / (E(3) + E(0))
+    vbar = (E(-10) * 3 + E(2) * 4) / (E(-10) + E(2))
+    assert abs(o_dense[0, 0] - ((1 - want) * o_kept + want * vbar)) < 1e-14
+    r = oracle.prefill(q[None, None], k[None, None], v[None, None], causal=False, lam=E(-0.5),
+                       tile_q=2, tile_k=2, scale=1.0)
+    assert abs(r.o[0, 0, 0, 0] - o_kept) < 1e-14
+    assert np.all(np.abs(o_dense[:, 0] - r.o[0, 0, :, 0]) <= eps * (4.0 - 1.0))
+
+
 def test_worked_prefill_causal():
     # Sq = Skv = 4, tiles 2x2; row i sees keys <= i.
     q = np.ones((1, 1, 4, 1))
