@@ -69,6 +69,23 @@ rounding of n decides a discrete value, keys whose exponent lies within
 POT_AMBIGUOUS_BAND of a rounding boundary are reported: a kernel computing the
 logits in fp32 may round them the other way.
 
+FP8 P.V (optional, prefill)
+---------------------------
+"Approximating Softmax in Pretrained LLMs ...", AI Summary: FP8/BF16 mixed-precision
+tensor cores.  With e4m3 Q, K and V the second product also runs in e4m3, so the
+softmax weights themselves are quantised.  Reading used here (the pages give no
+formula): on a kept tile, with m'_r the exact running row maximum after the tile,
+each weight p_rc = exp(s_rc - m'_r) <= 1 enters P.V as e4m3(2^8 * p_rc) * 2^-8 --
+scaled by 2^8 so that the largest weight, 1, maps to 256 (inside e4m3's 448) and every
+p >= 2^-14 keeps e4m3's three mantissa bits -- rounded to nearest, ties to even.  The
+row sum l takes the unquantised p (it is the softmax's denominator), and the earlier
+tiles are rescaled exactly by exp(m - m') when the maximum grows, as in the exact
+recurrence.  The skip vote is unchanged.  Keys whose 2^8 * p lies within a relative
+FP8_AMBIGUOUS_BAND of an e4m3 rounding midpoint are reported: fp32 arithmetic may
+round them to the neighbouring e4m3 value.  e4m3 rounding (OCP E4M3: 4 exponent bits of
+bias 7, 3 mantissa bits, subnormal step 2^-9, largest finite 448) is written out below
+from that definition.
+
 Everything is fp64; bf16 inputs convert to fp64 exactly.  There is no blocking,
 fusion or reordering beyond the tile loop that defines the method.
 """
@@ -86,6 +103,12 @@ LOG2E = 1.0 / math.log(2.0)
 # half-width (in log2 units) of the band around a rounding boundary of the
 # Rowmax-PoT exponent inside which an fp32 computation may round differently
 POT_AMBIGUOUS_BAND = 1e-4
+# relative half-width of the band around an e4m3 rounding midpoint inside which the
+# fp32 weights of the FP8 P.V product may round differently
+FP8_AMBIGUOUS_BAND = 2e-4
+# the FP8 P.V weights are quantised as e4m3(2^FP8_P_SHIFT * p) * 2^-FP8_P_SHIFT
+FP8_P_SHIFT = 8
+E4M3_MAX = 448.0
 
 
 # ---------------------------------------------------------------------------
@@ -163,6 +186,49 @@ def _online_update_pot(m: np.ndarray, l: np.ndarray, o: np.ndarray, a: np.ndarra
     return m_new, l_new, o_new, a_new
 
 
+def e4m3_step(y: np.ndarray) -> np.ndarray:
+    """Spacing of the e4m3 values around |y| (y finite): 2^(e-3) in the binade
+    [2^e, 2^(e+1)) for e >= -6, and the subnormal step 2^-9 below 2^-6."""
+    a = np.abs(y)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))     # a = f * 2^ex, f in [0.5, 1)
+    e = ex - 1
+    return np.where(a >= 2.0 ** -6, np.exp2(e - 3.0), 2.0 ** -9)
+
+
+def e4m3_round(y: np.ndarray) -> np.ndarray:
+    """Round to the nearest OCP E4M3 value, ties to even, saturating at +-448."""
+    y = np.asarray(y, dtype=np.float64)
+    q = e4m3_step(y)
+    r = np.rint(y / q) * q          # y / q is exact (a power-of-two scale); rint ties to even
+    return np.clip(r, -E4M3_MAX, E4M3_MAX)
+
+
+def _fp8_pv_weights(p: np.ndarray):
+    """(w, ambiguous): w = e4m3(2^8 p) 2^-8, ambiguous where 2^8 p is within a relative
+    FP8_AMBIGUOUS_BAND of an e4m3 rounding midpoint (p > 0)."""
+    y = p * 2.0 ** FP8_P_SHIFT
+    w = e4m3_round(y) * 2.0 ** -FP8_P_SHIFT
+    q = e4m3_step(y)
+    frac = y / q - np.floor(y / q)
+    amb = (np.abs(frac - 0.5) * q < FP8_AMBIGUOUS_BAND * y) & (p > 0)
+    return w, amb
+
+
+def _online_update_fp8_pv(m: np.ndarray, l: np.ndarray, o: np.ndarray, a: np.ndarray,
+                          s: np.ndarray, vtile: np.ndarray):
+    """The online update with e4m3-quantised weights in P.V (l keeps the exact weights);
+    `a` is the running weight, in the units of l, of keys with an ambiguous rounding."""
+    m_new = np.maximum(m, np.max(s, axis=1))
+    with np.errstate(invalid="ignore"):
+        alpha = np.where(m == NEG_INF, 0.0, np.exp(m - m_new))
+        p = np.where(s == NEG_INF, 0.0, np.exp(s - m_new[:, None]))
+    w, amb = _fp8_pv_weights(p)
+    l_new = alpha * l + p.sum(axis=1)
+    o_new = alpha[:, None] * o + w @ vtile
+    a_new = alpha * a + (p * amb).sum(axis=1)
+    return m_new, l_new, o_new, a_new
+
+
 def _finish(m: np.ndarray, l: np.ndarray, o: np.ndarray):
     return o / l[:, None], m + np.log(l)
 
@@ -197,12 +263,14 @@ def last_visible_key(r1: int, Sq: int, Skv: int, causal: bool) -> int:
 
 def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, tile_q: int,
                   tile_k: int, causal: bool, lam: float, scale: float, pot: bool = False,
-                  block_mask_row: Optional[np.ndarray] = None):
+                  block_mask_row: Optional[np.ndarray] = None, fp8_pv: bool = False):
     """One query tile of one head: returns (o_rows, lse_rows, mask[nkt], margin[nkt],
     ambiguous_fraction_rows or None).
 
     qh is the head's full query matrix [Sq][D]; kh, vh its kv head [Skv][D].  With
-    pot=True kept tiles take Rowmax-PoT weights instead of exact exponentials.
+    pot=True kept tiles take Rowmax-PoT weights instead of exact exponentials; with
+    fp8_pv=True their weights enter P.V quantised to e4m3 (the FP8 P.V reading above) and
+    the fifth result is the ambiguous fraction of that rounding.
     block_mask_row, if given, is a boolean [nkt] of the key tiles this query tile visits.
     """
     Sq, Skv = qh.shape[0], kh.shape[0]
@@ -231,11 +299,13 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
             continue
         if pot:
             m, l, o, a = _online_update_pot(m, l, o, a, s, vh[c0:c1])
+        elif fp8_pv:
+            m, l, o, a = _online_update_fp8_pv(m, l, o, a, s, vh[c0:c1])
         else:
             m, l, o = _online_update(m, l, o, s, vh[c0:c1])
     seen = l > 0.0                         # rows with at least one visited visible key
     lsafe = np.where(seen, l, 1.0)
-    amb = np.where(seen, a / lsafe, 0.0) if pot else None
+    amb = np.where(seen, a / lsafe, 0.0) if (pot or fp8_pv) else None
     o, lse = _finish(m, lsafe, o)
     o = np.where(seen[:, None], o, 0.0)
     lse = np.where(seen, lse, NEG_INF)
@@ -244,14 +314,19 @@ def prefill_qtile(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, t: int, *, til
 
 def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: float,
             tile_q: int, tile_k: int, scale: Optional[float] = None,
-            pot: bool = False, block_mask: Optional[np.ndarray] = None) -> PrefillResult:
+            pot: bool = False, block_mask: Optional[np.ndarray] = None,
+            fp8_pv: bool = False) -> PrefillResult:
     """Skip Softmax prefill over q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] (fp64); pot=True
-    uses Rowmax-PoT weights on kept tiles; block_mask, if given, is a boolean
+    uses Rowmax-PoT weights on kept tiles, fp8_pv=True e4m3-quantised weights in P.V
+    (pot_ambiguous then holds that rounding's ambiguous fraction); block_mask, if given,
+    is a boolean
     [B][Hq][nqt][nkt] of the (query tile, key tile) pairs to visit."""
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     if Hq % Hkv or (causal and Sq > Skv):
         raise ValueError("invalid shapes")
+    if pot and fp8_pv:
+        raise ValueError("pot and fp8_pv are separate readings")
     G = Hq // Hkv
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     nqt = (Sq + tile_q - 1) // tile_q
@@ -260,7 +335,7 @@ def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: f
     lse = np.zeros((B, Hq, Sq))
     mask = np.full((B, Hq, nqt, nkt), -1, dtype=np.int8)
     margin = np.full((B, Hq, nqt, nkt), np.inf)
-    amb = np.zeros((B, Hq, Sq)) if pot else None
+    amb = np.zeros((B, Hq, Sq)) if (pot or fp8_pv) else None
     for b in range(B):
         for h in range(Hq):
             kh, vh = k[b, h // G], v[b, h // G]
@@ -268,11 +343,11 @@ def prefill(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, causal: bool, lam: f
                 r0, r1 = t * tile_q, min((t + 1) * tile_q, Sq)
                 ot, lt, mt, gt, at = prefill_qtile(
                     q[b, h], kh, vh, t, tile_q=tile_q, tile_k=tile_k, causal=causal, lam=lam,
-                    scale=scale, pot=pot,
+                    scale=scale, pot=pot, fp8_pv=fp8_pv,
                     block_mask_row=None if block_mask is None else block_mask[b, h, t])
                 o[b, h, r0:r1], lse[b, h, r0:r1] = ot, lt
                 mask[b, h, t], margin[b, h, t] = mt, gt
-                if pot:
+                if pot or fp8_pv:
                     amb[b, h, r0:r1] = at
     return PrefillResult(o, lse, mask, margin, amb)
 
