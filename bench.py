@@ -517,7 +517,33 @@ def run_ours(args):
             "speedup_vs_bf16_lambda0": t_dense / sec,
             "max_abs_err_vs_bf16_lambda0": float(d.max()),
             "mean_abs_err_vs_bf16_lambda0": float(d.mean())})
-    del q8, k8
+    # all-e4m3 path: e4m3 V (transposed) and P quantised to e4m3 for P.V
+    v8t = v.to(torch.float8_e4m3fn).transpose(2, 3).contiguous()
+    sweep_fp8_pv = []
+    for lam in (0.0, lam_step):
+        def run_fp8_pv():
+            bs.prefill(q8, k8, v8t, lam, causal=True, out=o, skip_counts=cnt)
+        sec = time_events(run_fp8_pv, 3)
+        d = (o.float() - o_ref.float()).abs()
+        sk = int(cnt.sum().item())
+        sweep_fp8_pv.append({
+            "lambda": lam, "skip_ratio": sk / visited, "ms": sec * 1e3,
+            "dense_equiv_tflops": prefill_dense_flops(wp) / sec / 1e12,
+            "speedup_vs_bf16_lambda0": t_dense / sec,
+            "max_abs_err_vs_bf16_lambda0": float(d.max()),
+            "mean_abs_err_vs_bf16_lambda0": float(d.mean())})
+    del q8, k8, v8t
+    # V rows of a key tile fetched only once a query tile keeps it, against the default
+    # schedule that fetches every V tile ahead of the vote (identical results)
+    sweep_vload = []
+    for lam in (0.0, lam_pf[0.3], lam_step, lam_pf[0.7]):
+        row = {"lambda": lam}
+        for mode in ("ahead", "after_vote"):
+            def run_mode():
+                bs.prefill(q, k, v, lam, causal=True, out=o, skip_counts=cnt, v_load=mode)
+            row[f"ms_{mode}"] = time_events(run_mode, 3) * 1e3
+        row["skip_ratio"] = int(cnt.sum().item()) / visited
+        sweep_vload.append(row)
     # Skip Softmax behind a prefill block selector: a seeded mask keeps the diagonal and
     # the first key tile of every query tile and half of the others at random
     nqt_m = nqt
@@ -731,7 +757,7 @@ def run_ours(args):
     mhz = clocks.get("sm_mhz")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
                 "frac": achieved / burst, "traffic": profiled_traffic(PREFILL),
-                "kernel": "prefill_kernel<128,128,128,3,2,0,0,0>",
+                "kernel": "prefill_kernel<128,128,128,3,2,0,0,0,0>",
                 "peak_source": f"{src} bf16_tflops (cuBLAS 8192^3, best of 10: burst)",
                 # the same peak scaled to the clock this kernel ran at (median SM MHz of the
                 # timed region), taking the burst GEMM to have run at the maximum SM clock
@@ -758,6 +784,7 @@ def run_ours(args):
         "sweep": {"prefill": sweep_pf, "decode": sweep_dec, "prefill_rowmax_pot": sweep_pot,
                   "decode_splits": sweep_splits,
                   "decode_block_mask": sweep_bm, "prefill_fp8_qk": sweep_fp8,
+                  "prefill_fp8_qkv": sweep_fp8_pv, "prefill_v_load": sweep_vload,
                   "prefill_block_mask": sweep_pbm},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},

@@ -39,10 +39,20 @@ class PrefillOpts(ctypes.Structure):
                 ("wait_limit_ms", ctypes.c_int), ("exp_mode", ctypes.c_int),
                 ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float),
                 ("block_mask", ctypes.c_void_p), ("inject_wait_timeout", ctypes.c_int),
-                ("status", ctypes.c_void_p)]
+                ("status", ctypes.c_void_p), ("v_format", ctypes.c_int),
+                ("v_descale", ctypes.c_float), ("v_load", ctypes.c_int)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
+
+
+V_LOADS = {"default": 0, "ahead": 1, "after_vote": 2}
+
+
+def _v_load(v_load) -> int:
+    if v_load not in V_LOADS:
+        raise ValueError(f"v_load must be one of {sorted(V_LOADS)}")
+    return V_LOADS[v_load]
 
 
 def _exp_mode(exp_mode) -> int:
@@ -163,11 +173,15 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
             return_visited: bool = False, out=None, skip_counts=None, stream=None,
             wait_limit_ms: int = 0, exp_mode: str = "exact",
             qk_descale: float = 0.0, block_mask=None,
-            inject_wait_timeout: bool = False, status=None) -> PrefillOut:
+            inject_wait_timeout: bool = False, status=None,
+            v_descale: float = 0.0, v_load: str = "default") -> PrefillOut:
     """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
     q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
-    Q.K^T in e4m3, scaled by qk_descale); v is bf16.  exp_mode "exact" uses exponentials on
+    Q.K^T in e4m3, scaled by qk_descale); v is bf16 [B][Hkv][Skv][D], or, with e4m3 q and
+    k, float8_e4m3fn transposed to [B][Hkv][D][Skv] (P.V in e4m3 as well; the output is
+    multiplied by v_descale).  v_load: "default", "ahead" (every V tile before the vote) or
+    "after_vote" (only the V tiles of kept key tiles).  exp_mode "exact" uses exponentials on
     kept tiles, "pot" Rowmax-PoT powers of two.  block_mask: optional uint8/bool CUDA
     tensor [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)] of the pairs to visit.
     status: optional int32 CUDA tensor of one element that receives this call's
@@ -176,9 +190,12 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     import torch
     lib = library()
     fp8 = q.dtype == torch.float8_e4m3fn
-    _check_tensor("q", q, 4, fp8), _check_tensor("k", k, 4, fp8), _check_tensor("v", v, 4)
+    v8 = fp8 and v.dtype == torch.float8_e4m3fn
+    _check_tensor("q", q, 4, fp8), _check_tensor("k", k, 4, fp8), _check_tensor("v", v, 4, v8)
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
+    if v8 and tuple(v.shape) != (B, Hkv, D, Skv):
+        raise TypeError(f"e4m3 v must be transposed: shape {(B, Hkv, D, Skv)}")
     tq = tile_q or (64 if D == 64 else 128)
     tk = tile_k or (64 if D == 64 else 128)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if out is None else out
@@ -197,7 +214,8 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     opts = PrefillOpts(tq, tk, float(softmax_scale), ptr(lse).value, ptr(mask).value,
                        ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
                        float(qk_descale), ptr(block_mask).value,
-                       1 if inject_wait_timeout else 0, _status_ptr(status))
+                       1 if inject_wait_timeout else 0, _status_ptr(status), 1 if v8 else 0,
+                       float(v_descale), _v_load(v_load))
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))

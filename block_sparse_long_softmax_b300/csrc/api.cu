@@ -243,6 +243,16 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
     return fail(SKIPSM_ERR_UNSUPPORTED, "e4m3 q/k need D = 128 and tile_k = 128");
   if (!(op.qk_descale >= 0.f) || !std::isfinite(op.qk_descale))
     return fail(SKIPSM_ERR_INVALID_ARG, "qk_descale must be finite and >= 0");
+  if (op.v_format != 0 && op.v_format != 1)
+    return fail(SKIPSM_ERR_INVALID_ARG, "v_format must be 0 (bf16) or 1 (e4m3, transposed)");
+  if (op.v_format == 1 && (op.qk_format != 1 || op.exp_mode != 0))
+    return fail(SKIPSM_ERR_UNSUPPORTED, "e4m3 v needs e4m3 q/k and exact exponentials");
+  if (op.v_format == 1 && Skv % 16)
+    return fail(SKIPSM_ERR_UNSUPPORTED, "e4m3 v needs Skv to be a multiple of 16 (row stride)");
+  if (!(op.v_descale >= 0.f) || !std::isfinite(op.v_descale))
+    return fail(SKIPSM_ERR_INVALID_ARG, "v_descale must be finite and >= 0");
+  if (op.v_load < 0 || op.v_load > 2)
+    return fail(SKIPSM_ERR_INVALID_ARG, "v_load must be 0, 1 or 2");
   const long long nblk_q = (Sq + 255) / 256;
   if (nblk_q * B * Hq > 0x7FFFFFFFLL) return fail(SKIPSM_ERR_UNSUPPORTED, "grid too large");
   int* status = op.status ? op.status : device_status_word();
@@ -254,7 +264,12 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   const int qk_elem = op.qk_format == 1 ? 1 : 2;
   if ((st = make_map(&qmap, q, D, Sq, static_cast<long long>(B) * Hq, 128, qk_elem))) return st;
   if ((st = make_map(&kmap, k, D, Skv, static_cast<long long>(B) * Hkv, tk, qk_elem))) return st;
-  if ((st = make_map(&vmap, v, D, Skv, static_cast<long long>(B) * Hkv, tk))) return st;
+  if (op.v_format == 1) {
+    // v^T [B*Hkv][D][Skv]: boxes of 128 keys (one 128-byte atom) by D rows
+    if ((st = make_map(&vmap, v, Skv, D, static_cast<long long>(B) * Hkv, D, 1))) return st;
+  } else if ((st = make_map(&vmap, v, D, Skv, static_cast<long long>(B) * Hkv, tk))) {
+    return st;
+  }
 
   PrefillParams p;
   std::memset(&p, 0, sizeof(p));
@@ -269,6 +284,9 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   set_lambda(lambda, &p.lam_log2, &p.lam_pos);
   p.qk_e4m3 = op.qk_format == 1 ? 1 : 0;
+  p.v_e4m3 = op.v_format == 1 ? 1 : 0;
+  p.v_descale = op.v_descale > 0.f ? op.v_descale : 1.f;
+  p.v_after_vote = op.v_load == 2 ? 1 : 0;
   p.block_mask = op.block_mask;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = op.lse;

@@ -27,6 +27,7 @@ enum WaitSite : int {
   kSitePrefillODone = 23,
   kSitePrefillDrain = 24,
   kSitePrefillInjected = 25,
+  kSitePrefillVDec = 26,
 };
 
 struct DecodeParams {
@@ -72,7 +73,10 @@ struct PrefillParams {
   float lam_log2;
   int lam_pos;
   int exp_mode;          // 0 exact exponentials, 1 Rowmax-PoT weights
-  int qk_e4m3;           // Q and K are e4m3 (V stays bf16)
+  int qk_e4m3;           // Q and K are e4m3
+  int v_e4m3;            // V is e4m3, transposed [B][Hkv][D][Skv] (needs qk_e4m3)
+  float v_descale;       // multiplies the output (the caller's V quantisation scale)
+  int v_after_vote;      // load V_j only once a Q tile keeps key tile j
   const uint8_t* block_mask;  // [B][Hq][nqt][nkt] pairs to visit, or null for all
   int inject_fault;      // test hook: the softmax warps wait on a barrier nothing arrives at
   __nv_bfloat16* o;      // [B][Hq][Sq][D]

@@ -30,6 +30,9 @@
 // The running max used by the vote is always the exact prefix max; the
 // accumulator's reference max is only moved when the max has grown by more
 // than 2^8 (lazy rescaling), which changes no result.
+// With e4m3 Q, K and V the weights of P.V are quantised to e4m3 relative to the
+// exact running max (the reference then follows it on every increase) and P goes
+// to shared memory, one buffer per Q tile, as the A operand of an e4m3 MMA.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tmem_wide.cuh"
@@ -40,6 +43,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kQRows = 128;        // rows of one Q tile (= MMA M)
 constexpr float kRescaleLog2 = 8.f;
+// e4m3 P.V: the weights enter the MMA as e4m3(2^kPShift * p), p <= 1, so the largest maps
+// to 256 (inside e4m3's range) and every p >= 2^-14 keeps three mantissa bits
+constexpr float kPShift = 8.f;
+constexpr int kNDec = 4;   // ring of per-key-tile V decisions (V loads after the vote)
 
 // Test-only instrumentation (built with -DSKIPSM_TRACE=1 into a separate library):
 // one lane of the softmax warp of TMEM quadrant 0 and of the MMA warp stamp clock64
@@ -54,26 +61,33 @@ constexpr float kRescaleLog2 = 8.f;
 #define SKIPSM_STAMP(on, j, x, e, val) do { } while (0)
 #endif
 
-template <int D, int BK, int TQ, int NK, int NV, bool F8>
+// F8: 0 = bf16 Q/K/V; 1 = e4m3 Q and K, bf16 V; 2 = e4m3 Q and K and e4m3 V given
+// transposed (keys innermost), with P quantised to e4m3 for the second product.
+template <int D, int BK, int TQ, int NK, int NV, int F8>
 struct PrefillCfg {
-  // Q and K are bf16, or e4m3 with F8; V is always bf16.  Operand rows are cut into
-  // 128-byte swizzle atoms along D: kAtoms of them, kAtomElems elements each.
+  static constexpr bool kV8 = F8 == 2;
+  // Operand rows are cut into 128-byte swizzle atoms along D: kAtoms of them,
+  // kAtomElems elements each.
   static constexpr int kQKElem = F8 ? 1 : 2;
   static constexpr int kAtoms = D * kQKElem / 128;
   static constexpr int kAtomElems = 128 / kQKElem;
   static constexpr int kQTileBytes = kQRows * D * kQKElem;
   static constexpr int kKBytes = BK * D * kQKElem;
-  static constexpr int kVBytes = BK * D * 2;
+  static constexpr int kVBytes = BK * D * (kV8 ? 1 : 2);
+  static constexpr int kPBytes = kV8 ? kQRows * BK : 0;    // e4m3 P of one Q tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * kQTileBytes;
   static constexpr int kOffV = kOffK + NK * kKBytes;
-  static constexpr int kOffBar = kOffV + NV * kVBytes;
+  static constexpr int kOffP = kOffV + NV * kVBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
   // barriers: qfull, kfull[NK], kempty[NK], vfull[NV], vempty[NV], sfull[2],
   //           pfull[2], odone[2], final, never (failure-detection test hook)
-  static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 2;
+  //           vdec[kNDec] (V loads after the vote)
+  static constexpr int kNBar = 1 + 2 * NK + 2 * NV + 6 + 2 + kNDec;
   static constexpr int kOffVote = kOffBar + kNBar * 8;       // [2 x][2 parity][4 warps] int
   static constexpr int kOffDec = kOffVote + 2 * 2 * 4 * 4;   // [2] int
-  static constexpr int kOffTmem = kOffDec + 2 * 4;           // uint32
+  static constexpr int kOffNeed = kOffDec + 2 * 4;           // [kNDec] int
+  static constexpr int kOffTmem = kOffNeed + kNDec * 4;      // uint32
   static constexpr int kOffAbort = kOffTmem + 4;
   static constexpr int kBytes = kOffAbort + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -82,9 +96,13 @@ struct PrefillCfg {
   static constexpr int kTmemUsed = 2 * BK + 2 * D;
   static constexpr uint32_t kTmemCols = kTmemUsed <= 256 ? 256u : 512u;
   static constexpr uint32_t kIdescQK = F8 ? idesc_e4m3(kQRows, BK) : idesc_bf16(kQRows, BK, false, false);
-  static constexpr uint32_t kIdescPV = idesc_bf16(kQRows, D, false, true);
+  // P.V: A = P (TMEM, or e4m3 in shared memory), B = V MN-major (bf16) or V^T K-major (e4m3)
+  static constexpr uint32_t kIdescPV = kV8 ? idesc_e4m3(kQRows, D) : idesc_bf16(kQRows, D, false, true);
+  static constexpr float kRescale = kV8 ? 0.f : kRescaleLog2;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!F8 || D == 128, "e4m3 Q/K: one 128-byte atom per row needs D = 128");
+  static_assert(!kV8 || BK == 128, "e4m3 V: one 128-byte atom of keys per row needs BK = 128");
+  static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
   static_assert(BK == 64 || BK == 128, "key tile");
   static_assert(TQ == 64 || TQ == 128, "vote rows");
   static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -129,17 +147,22 @@ __device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[
 template <>
 __device__ __forceinline__ void tmem_st<64>(uint32_t taddr, const uint32_t (&r)[64]) { tmem_st64(taddr, r); }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8, bool BM>
+// VE: V_j is loaded only once a Q tile of the CTA has voted to keep key tile j (the
+// softmax posts one decision per key tile); otherwise every V_j is loaded ahead.
+template <int D, int BK, int TQ, int NK, int NV, bool POT, int F8, bool BM, bool VE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using C = PrefillCfg<D, BK, TQ, NK, NV, F8>;
+  constexpr bool V8 = C::kV8;
+  static_assert(!(VE && POT), "the Rowmax-PoT MMA loop waits for V before the votes");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
+  const uint32_t sP = sbase + C::kOffP;   // e4m3 P of Q tile x at sP + x * kPBytes
   const uint32_t bar0 = sbase + C::kOffBar;
   const uint32_t qfull = bar0;
   auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -151,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto odone = [&](int x) { return bar0 + 8u * (5 + 2 * NK + 2 * NV + x); };
   const uint32_t final_bar = bar0 + 8u * (7 + 2 * NK + 2 * NV);
   const uint32_t never_bar = bar0 + 8u * (8 + 2 * NK + 2 * NV);  // nothing arrives here
+  auto vdec = [&](int i) { return bar0 + 8u * (9 + 2 * NK + 2 * NV + i); };
+  volatile int* sneed = reinterpret_cast<volatile int*>(smem + C::kOffNeed);
   int* svote = reinterpret_cast<int*>(smem + C::kOffVote);
   volatile int* sdec = reinterpret_cast<volatile int*>(smem + C::kOffDec);
   uint32_t* stmem = reinterpret_cast<uint32_t*>(smem + C::kOffTmem);
@@ -185,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(final_bar, 1);
     mbar_init(never_bar, 1);
+    for (int i = 0; i < kNDec; ++i) mbar_init(vdec(i), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -217,20 +243,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull,
                         h * C::kAtomElems, qrow0 + x * kQRows, zq);
       }
+      // with VE the V ring holds only the kept tiles, in order: the n-th loaded V tile
+      // uses stage n % NV
+      const bool elide = VE && !is_k;
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
-        const int st = j % NS;
+        if (elide) {
+          if (!mbar_wait(vdec(j % kNDec), (j / kNDec) & 1, wc, kSitePrefillVDec)) break;
+          if (!sneed[j % kNDec]) continue;
+        }
+        const int n = elide ? issued : j;
+        const int st = n % NS;
         const uint32_t empty = is_k ? kempty(st) : vempty(st);
         const uint32_t full = is_k ? kfull(st) : vfull(st);
-        if (j >= NS && !mbar_wait(empty, ((j / NS) - 1) & 1, wc,
+        if (n >= NS && !mbar_wait(empty, ((n / NS) - 1) & 1, wc,
                                   is_k ? kSitePrefillKEmpty : kSitePrefillVEmpty))
           break;
         const int bytes = is_k ? C::kKBytes : C::kVBytes;
         const int atoms = is_k ? C::kAtoms : D / 64;
         const int atom_elems = is_k ? C::kAtomElems : 64;
         mbar_arrive_expect_tx(full, bytes);
-        for (int h = 0; h < atoms; ++h)
-          tma_load_3d(ring + st * bytes + h * BK * 128, map, full, h * atom_elems, j * BK, zk);
+        if (V8 && !is_k) {
+          // V^T: rows are the D dimensions, each one 128-byte atom of the tile's keys
+          tma_load_3d(ring + st * bytes, map, full, j * BK, 0, zk);
+        } else {
+          for (int h = 0; h < atoms; ++h)
+            tma_load_3d(ring + st * bytes + h * BK * 128, map, full, h * atom_elems, j * BK, zk);
+        }
         ++issued;
       }
       if (*abort_flag) {
@@ -264,18 +303,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           // advance the start address (16-byte units) within / across swizzle atoms
           const uint32_t qo = ((kk >> 2) * (kQRows * 128) + (kk & 3) * 32) >> 4;
           const uint32_t ko = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-          if constexpr (F8)
+          if constexpr (F8 != 0)
             umma_ss_f8_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
           else
             umma_ss_w(tmem + colS[x], qd + qo, kd + ko, C::kIdescQK, kk > 0 ? 1u : 0u, issue);
         }
       };
       auto issue_pv = [&](int x, int vs) {
-        const uint64_t vd = sdesc_sw128(sV + vs * C::kVBytes, BK * 128, 1024);
+        if constexpr (V8) {
+          // A = e4m3 P of Q tile x (one 128-byte atom of keys per row), B = V^T (one atom of
+          // keys per D row); each MMA covers 32 keys
+          const uint64_t pd = sdesc_sw128(sP + x * C::kPBytes, 16, 1024);
+          const uint64_t vd = sdesc_sw128(sV + vs * C::kVBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          umma_ts_w(tmem + colO[x], tmem + colS[x] + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                    C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u, issue);
+          for (int kk = 0; kk < BK / 32; ++kk)
+            umma_ss_f8_w(tmem + colO[x], pd + kk * 2, vd + kk * 2, C::kIdescPV,
+                         (first_pv[x] && kk == 0) ? 0u : 1u, issue);
+        } else {
+          const uint64_t vd = sdesc_sw128(sV + vs * C::kVBytes, BK * 128, 1024);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_ts_w(tmem + colO[x], tmem + colS[x] + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                      C::kIdescPV, (first_pv[x] && kk == 0) ? 0u : 1u, issue);
+        }
         first_pv[x] = false;
       };
       bool ok = wait(qfull, 0, kSitePrefillQ) && wait(kfull(0), 0, kSitePrefillKFull);
@@ -293,8 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #else
       const bool tr_on = false;
 #endif
+      (void)tr_on;
+      int nv = 0;  // with VE: V tiles consumed (only kept tiles are loaded)
       for (int j = 0; ok && j < nmax; ++j) {
-        const int vs = j % NV, ks1 = (j + 1) % NK;
+        const int vn = VE ? nv : j;   // the producer's count of V tiles before this one
+        const int vs = vn % NV, ks1 = (j + 1) % NK;
+        const uint32_t vpar = (vn / NV) & 1;
         const bool has_next = j + 1 < nmax;
         bool v_ready = false, k_ready = false;
         if constexpr (POT) {
@@ -303,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // between that P and its MMAs) measured 3-4 % faster on the 128K prefill; with
           // exact exponentials it measured 1 % slower at lambda = 0, so the exact kernel
           // waits for each where it first uses it.
-          if (!wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) { ok = false; break; }
+          if (!wait(vfull(vs), vpar, kSitePrefillVFull)) { ok = false; break; }
           v_ready = true;
           if (has_next) {
             if (!wait(kfull(ks1), ((j + 1) / NK) & 1, kSitePrefillKFull)) { ok = false; break; }
@@ -319,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           SKIPSM_STAMP(tr_on, j, x, 9, clock64());
           if (sdec[x]) {
             if (!v_ready) {
-              if (!wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) { ok = false; break; }
+              if (!wait(vfull(vs), vpar, kSitePrefillVFull)) { ok = false; break; }
               v_ready = true;
               tc_fence_after();
             }
@@ -342,8 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (has_next) umma_commit_w(kempty(ks1), issue);
-        if (!v_ready && !wait(vfull(vs), (j / NV) & 1, kSitePrefillVFull)) break;
-        umma_commit_w(vempty(vs), issue);
+        if constexpr (VE) {
+          // V_j was loaded iff some Q tile kept tile j
+          if (v_ready) {
+            umma_commit_w(vempty(vs), issue);
+            ++nv;
+          }
+        } else {
+          if (!v_ready && !wait(vfull(vs), vpar, kSitePrefillVFull)) break;
+          umma_commit_w(vempty(vs), issue);
+        }
       }
       // every MMA issued by this warp completes before TMEM is released
       umma_commit_w(final_bar, issue);
@@ -391,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tr[x].l = 0.f;
     }
     unsigned long long n_skip = 0, n_visit = 0;
+    int v_posted = -1;   // (thread 0, VE) the last key tile whose V decision is posted
     bool ok = true;
     if (p.inject_fault) {
       // failure-detection test hook: a wait on a barrier nothing arrives at, with half
@@ -403,6 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #else
     const bool tr_on = false;
 #endif
+    (void)tr_on;
+    // e4m3 P row of Q tile x into shared memory: eight 16-byte chunks of 16 keys,
+    // XOR-swizzled within the row's 128-byte atom (the MMA's 128-byte-swizzle layout).
+    // P_x(j) is free to overwrite: its S was committed after the P.V that read P_x(j-1).
+    auto store_p8 = [&](int x, const uint32_t (&pk)[BK / 2]) {
+      const uint32_t row = sP + x * C::kPBytes + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(row + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                     pk[4 * c + 3]);
+      fence_proxy_async_smem();
+    };
     bool next_ready = false;  // the S of the next tile in this order is known to be complete
     // The softmax of one (Q tile x, key tile j): t is the row state of Q tile x, o that of the
     // other Q tile.
@@ -506,13 +581,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.skip_mask[((static_cast<size_t>(b) * p.Hq + hq) * p.nqt + t.qtile) * p.nkt + j] =
               my_skip ? 1 : 0;
       }
-      if (r == 0) sdec[x] = any_kept ? 1 : 0;
+      if (r == 0) {
+        sdec[x] = any_kept ? 1 : 0;
+        if constexpr (VE) {
+          // V_j is fetched once some Q tile keeps tile j: at the first Q tile that keeps it,
+          // or at the last Q tile that visits it
+          const bool last_visit = x == 1 || j >= n1;
+          if (v_posted != j && (any_kept || last_visit)) {
+            sneed[j % kNDec] = any_kept ? 1 : 0;
+            mbar_arrive(vdec(j % kNDec));
+            v_posted = j;
+          }
+        }
+      }
       if (any_kept) {
         if (!my_skip) {
           t.M = fmaxf(t.M, mt2);
           float alpha = 1.f;
           bool resc = false;
-          if (t.M > t.R + kRescaleLog2) {   // also true for the first kept tile (R = -inf)
+          if (t.M > t.R + C::kRescale) {   // also true for the first kept tile (R = -inf)
             resc = t.R != -INFINITY;
             alpha = ex2(t.R - t.M);
             t.l *= alpha;
@@ -534,7 +621,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float la[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[BK / 2];
-          if constexpr (!POT) {
+          if constexpr (V8) {
+            // P = 2^(s*scale*log2e - M + 8) rounded to e4m3 (the 2^8 cancels in O / l),
+            // written to shared memory in the 128-byte-swizzle layout of a K-major operand
+            float negR = kPShift - t.R;
+            if constexpr (BM) negR = t.R == -INFINITY ? 0.f : negR;
+#pragma unroll
+            for (int i = 0; i < BK / 4; ++i) {
+              float x0, x1, x2, x3;
+              ffma2(x0, x1, __uint_as_float(sv[4 * i]), __uint_as_float(sv[4 * i + 1]), sl2, negR);
+              ffma2(x2, x3, __uint_as_float(sv[4 * i + 2]), __uint_as_float(sv[4 * i + 3]), sl2, negR);
+              const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+              fadd2_acc(la[0], la[1], e0, e1);
+              fadd2_acc(la[2], la[3], e2, e3);
+              pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+            }
+          } else if constexpr (!POT) {
             // P = 2^(s*scale*log2e - R) in bf16, written over S (a row that has
             // seen no key yet, R = -inf, only has masked keys here: P = 0)
             float negR = -t.R;
@@ -578,12 +680,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           t.l += (la[0] + la[1]) + (la[2] + la[3]);
-          tmem_st<BK / 2>(tS, pk);
+          if constexpr (V8) {
+            store_p8(x, pk);
+          } else {
+            tmem_st<BK / 2>(tS, pk);
+          }
         } else {
           uint32_t z[BK / 2];
 #pragma unroll
           for (int i = 0; i < BK / 2; ++i) z[i] = 0u;
-          tmem_st<BK / 2>(tS, z);
+          if constexpr (V8) {
+            store_p8(x, z);
+          } else {
+            tmem_st<BK / 2>(tS, z);
+          }
         }
       }
       SKIPSM_STAMP(tr_on, j, x, 4, clock64());
@@ -636,7 +746,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           float inv = 1.f / t.l;
           __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row) * D;
           uint4* dst = reinterpret_cast<uint4*>(orow);
-          float lse2 = t.R + __log2f(t.l);
+          // (e4m3 P.V: l carries the 2^8 of the weights, and O the caller's V scale)
+          float lse2 = t.R + __log2f(t.l) - (V8 ? kPShift : 0.f);
+          if constexpr (V8) inv *= p.v_descale;
           if constexpr (BM) {
             // a row with no visited visible key (block mask) has l = 0: output 0, LSE -inf
             if (!(t.l > 0.f)) {
@@ -674,11 +786,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BK, int TQ, int NK, int NV, bool POT, bool F8, bool BM>
+template <int D, int BK, int TQ, int NK, int NV, bool POT, int F8, bool BM, bool VE = false>
 cudaError_t launch_cfg(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        const PrefillParams& p, cudaStream_t stream) {
   using C = PrefillCfg<D, BK, TQ, NK, NV, F8>;
-  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT, F8, BM>;
+  auto kern = prefill_kernel<D, BK, TQ, NK, NV, POT, F8, BM, VE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.nblk_q) * p.B * p.Hq;
@@ -701,7 +813,16 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
   }
 #define SKIPSM_PREFILL_CASE(d, bk, tq, nk, nv)                                 \
   if (p.D == d && p.tile_k == bk && p.tile_q == tq && !p.qk_e4m3)          \
-    SKIPSM_PREFILL_FLAGS(d, bk, tq, nk, nv, false)
+    SKIPSM_PREFILL_FLAGS(d, bk, tq, nk, nv, 0)
+  // V loads after the vote (bf16, D = 128, 128-key tiles, exact exponentials)
+  if (p.v_after_vote && p.D == 128 && p.tile_k == 128 && !p.qk_e4m3 && p.exp_mode == 0) {
+    const bool bm = p.block_mask != nullptr;
+    if (p.tile_q == 128)
+      return bm ? launch_cfg<128, 128, 128, 3, 2, false, 0, true, true>(qmap, kmap, vmap, p, stream)
+                : launch_cfg<128, 128, 128, 3, 2, false, 0, false, true>(qmap, kmap, vmap, p, stream);
+    return bm ? launch_cfg<128, 128, 64, 3, 2, false, 0, true, true>(qmap, kmap, vmap, p, stream)
+              : launch_cfg<128, 128, 64, 3, 2, false, 0, false, true>(qmap, kmap, vmap, p, stream);
+  }
   SKIPSM_PREFILL_CASE(128, 128, 128, 3, 2)
   SKIPSM_PREFILL_CASE(128, 128, 64, 3, 2)
   SKIPSM_PREFILL_CASE(128, 64, 128, 4, 4)
@@ -711,9 +832,18 @@ cudaError_t launch_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap,
   SKIPSM_PREFILL_CASE(64, 64, 128, 6, 6)
   SKIPSM_PREFILL_CASE(64, 64, 64, 6, 6)
   // e4m3 Q and K: 128-row vote groups or 64, 128-key tiles, D = 128
-  if (p.qk_e4m3 && p.D == 128 && p.tile_k == 128) {
-    if (p.tile_q == 128) SKIPSM_PREFILL_FLAGS(128, 128, 128, 4, 3, true)
-    SKIPSM_PREFILL_FLAGS(128, 128, 64, 4, 3, true)
+  if (p.qk_e4m3 && !p.v_e4m3 && p.D == 128 && p.tile_k == 128) {
+    if (p.tile_q == 128) SKIPSM_PREFILL_FLAGS(128, 128, 128, 4, 3, 1)
+    SKIPSM_PREFILL_FLAGS(128, 128, 64, 4, 3, 1)
+  }
+  // e4m3 Q, K and V (exact exponentials quantised to e4m3 for P.V)
+  if (p.qk_e4m3 && p.v_e4m3 && p.D == 128 && p.tile_k == 128 && p.exp_mode == 0) {
+    const bool bm = p.block_mask != nullptr;
+    if (p.tile_q == 128)
+      return bm ? launch_cfg<128, 128, 128, 4, 3, false, 2, true>(qmap, kmap, vmap, p, stream)
+                : launch_cfg<128, 128, 128, 4, 3, false, 2, false>(qmap, kmap, vmap, p, stream);
+    return bm ? launch_cfg<128, 128, 64, 4, 3, false, 2, true>(qmap, kmap, vmap, p, stream)
+              : launch_cfg<128, 128, 64, 4, 3, false, 2, false>(qmap, kmap, vmap, p, stream);
   }
 #undef SKIPSM_PREFILL_CASE
 #undef SKIPSM_PREFILL_FLAGS

@@ -127,6 +127,23 @@ typedef struct skipsm_prefill_opts {
                              writer wins) instead of in the library's shared word.  The call
                              neither clears nor reads it: zero it before the call, read it after
                              the stream has finished.  NULL = the shared word (skipsm_check) */
+  int v_format;           /* element type and layout of v: 0 = bf16 [B][Hkv][Skv][D];
+                             1 = e4m3, transposed: [B][Hkv][D][Skv], keys innermost (the
+                             K-major operand of the e4m3 tensor-core product; Skv a multiple
+                             of 16), with qk_format = 1, D = 128, tile_k = 128 and
+                             exp_mode = 0 only.  Then P.V runs in e4m3 too: on a kept tile each
+                             weight p = exp(s - m') (m' the exact running row max after the
+                             tile) enters it as e4m3(2^8 p) / 2^8, rounded to nearest even,
+                             while the row sum keeps the fp32 p ("Approximating Softmax in
+                             Pretrained LLMs: ...", AI Summary: FP8/BF16 mixed precision) */
+  float v_descale;        /* with v_format = 1: multiplies the output (the caller's v
+                             quantisation scale); 0 = 1 */
+  int v_load;             /* when the kernel fetches a key tile's V rows ("NVIDIA Introduces Skip
+                             Softmax ...", "Benefits and Implementation": a skipped block need
+                             not be read): 0 = the library's choice (currently 1); 1 = every V
+                             tile, ahead of the vote; 2 = only once a query tile of the CTA keeps
+                             the key tile (bf16 v, D = 128, tile_k = 128, exp_mode = 0; other
+                             configurations fall back to 1).  Results are identical. */
 } skipsm_prefill_opts;
 
 /*

@@ -48,7 +48,7 @@ def traced_prefill(lib, q, k, v, lam, cta):
     buf = torch.zeros(nkt * 2 * EV, dtype=torch.int64, device=q.device)
     o = torch.empty_like(q)
     mask = torch.empty((B, Hq, -(-Sq // 128), nkt), dtype=torch.uint8, device=q.device)
-    opts = bs.PrefillOpts(128, 128, 0.0, None, mask.data_ptr(), None, 0, 0, 0, 0.0, None, 0, None)
+    opts = bs.PrefillOpts(128, 128, 0.0, None, mask.data_ptr(), None, 0, 0, 0, 0.0, None, 0, None, 0, 0.0)
     lib.skipsm_debug_prefill_trace(buf.data_ptr(), cta)
     s = torch.cuda.current_stream().cuda_stream
     rc = lib.skipsm_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq,
