@@ -831,20 +831,31 @@ def run_kernel_only(args):
     w = synth.WORKLOADS[args.workload]
     q, k, v, _ = sdev.make_inputs(w)
     torch.cuda.synchronize()
+    lam = args.lam
+    if args.rho is not None:
+        # lambda for a target skip ratio first (the library's calibration: 14 launches)
+        if args.kernel_only == "prefill":
+            lam = bs.calibrate_prefill(q, k, v, args.rho, causal=w.causal, tile_q=w.tile_q,
+                                       tile_k=w.tile_k)[0]
+        else:
+            lam = bs.calibrate_decode(q, k, v, args.rho)[0]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.iters + 1)]
     for i in range(args.iters):
         ev[i].record()
         if args.kernel_only == "prefill":
-            out = bs.prefill(q, k, v, args.lam, causal=w.causal, tile_q=w.tile_q, tile_k=w.tile_k)
+            out = bs.prefill(q, k, v, lam, causal=w.causal, tile_q=w.tile_q, tile_k=w.tile_k,
+                             return_visited=True)
         else:
-            out = bs.decode(q, k, v, args.lam)
+            out = bs.decode(q, k, v, lam)
     ev[-1].record()
     torch.cuda.synchronize()
     status = bs.check()
     ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.iters)]
-    print(json.dumps({"kernel_only": args.kernel_only, "workload": w.name, "lambda": args.lam,
-                      "ms_per_launch": ms, "skipped": int(out.skip_counts.sum().item()),
-                      "status": status}))
+    line = {"kernel_only": args.kernel_only, "workload": w.name, "lambda": lam,
+            "ms_per_launch": ms, "skipped": int(out.skip_counts.sum().item()), "status": status}
+    if args.kernel_only == "prefill":
+        line["skip_ratio"] = line["skipped"] / int(out.visited_counts.sum().item())
+    print(json.dumps(line))
     return 0 if status == 0 else 1
 
 
@@ -922,6 +933,8 @@ def main(argv=None):
                     help="only launch this kernel on --workload (for profiler captures)")
     ap.add_argument("--workload", default=PREFILL)
     ap.add_argument("--lam", type=float, default=1e-3)
+    ap.add_argument("--rho", type=float, default=None,
+                    help="with --kernel-only: calibrate lambda to this skip ratio first")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--configs", action="store_true",
                     help="time every workload configuration at each of its lambda values")
