@@ -73,6 +73,9 @@ SMALL = [
     (dict(B=1, Hq=8, Hkv=1, Sq=129, Skv=129, D=64, window=32), 64, 64),
     (dict(B=1, Hq=1, Hkv=1, Sq=1, Skv=1, D=128, window=0, sink=1), 128, 128),
     (dict(B=1, Hq=1, Hkv=1, Sq=1, Skv=300, D=64, window=64), 64, 128),
+    # non-causal with more queries than keys: every query tile sees the whole (ragged) cache
+    (dict(B=1, Hq=2, Hkv=1, Sq=777, Skv=300, D=128, window=128, causal=False), 128, 128),
+    (dict(B=1, Hq=2, Hkv=2, Sq=333, Skv=65, D=64, window=32, causal=False), 64, 64),
 ]
 
 
