@@ -20,6 +20,7 @@ __device__ int g_device_status = 0;
 // `g_trace_cta` into `g_trace_buf` (see skipsm_debug_prefill_trace).
 unsigned long long* g_trace_buf = nullptr;
 int g_trace_cta = -1;
+unsigned long long* g_decode_trace_buf = nullptr;
 #endif
 
 namespace {
@@ -187,6 +188,12 @@ int skipsm_version(void) { return SKIPSM_VERSION; }
 void skipsm_debug_prefill_trace(void* buf, int cta) {
   g_trace_buf = static_cast<unsigned long long*>(buf);
   g_trace_cta = cta;
+}
+// Only in SKIPSM_TRACE builds: later decode calls record the start and end times
+// (%globaltimer, ns) of every split CTA into `buf` (device, [B][Hkv][splits][2] uint64);
+// buf = NULL stops recording.  Not part of the library's interface.
+void skipsm_debug_decode_trace(void* buf) {
+  g_decode_trace_buf = static_cast<unsigned long long*>(buf);
 }
 #endif
 
@@ -422,6 +429,9 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
   p.wait_cycles = wait_cycles(op.wait_limit_ms);
   p.inject_fault = op.inject_wait_timeout ? 1 : 0;
   p.block_mask = op.block_mask;
+#if SKIPSM_TRACE
+  p.trace = g_decode_trace_buf;
+#endif
   cudaError_t e;
   if (p.block_mask) {
     int dev = 0, optin = 0;

@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#if SKIPSM_TRACE
+  const size_t cta_lin = (static_cast<size_t>(b) * p.Hkv + hkv) * p.nsplit + split;
+  if (p.trace && threadIdx.x == 0) p.trace[2 * cta_lin] = globaltimer_ns();
+#endif
   const int j0 = split * p.per;
   const int nb = min(p.per, p.nblk - j0);
   const WaitCtx wc{p.wait_cycles, p.status, abort_flag};
@@ -347,6 +351,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int h = 0; h < G; ++h)
       atomicAdd(p.skip_counts + hkv * G + h, static_cast<unsigned long long>(n_skip));
   }
+#if SKIPSM_TRACE
+  if (p.trace && threadIdx.x == 0) p.trace[2 * cta_lin + 1] = globaltimer_ns();
+#endif
 }
 
 // One CTA per (b, query head); thread d merges dimension d over the splits.

@@ -47,6 +47,11 @@ struct DecodeParams {
   long long wait_cycles;
   int inject_fault;  // test hook: wait on a barrier nothing arrives at
   const uint8_t* block_mask;  // [B][Hkv][nblk] tiles to visit, or null for all
+#if SKIPSM_TRACE
+  // test-only instrumentation (SKIPSM_TRACE builds): %globaltimer at the start and the end
+  // of every split CTA, [linear CTA index][2]
+  unsigned long long* trace;
+#endif
 };
 
 struct CombineParams {

@@ -41,6 +41,13 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float e0, float e1, float e2, fl
   return r;
 }
 
+// The GPU's global nanosecond timer (the same clock on every SM).
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // 16-byte store to shared memory
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

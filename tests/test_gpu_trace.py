@@ -113,3 +113,78 @@ def test_trace_stamps_are_ordered_and_match_the_mask(lam):
             assert st[j, x, 9] >= st[j, x, 5] - 2000  # P is seen after (about) its arrive
             assert st[j, x, 11] >= st[j, x, 10]
     print(f"lambda={lam}: per-step median cycles", summarize(st, cm))
+
+
+def decode_trace_library():
+    lib = trace_library()
+    lib.skipsm_debug_decode_trace.argtypes = [ctypes.c_void_p]
+    lib.skipsm_decode_ex.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+         ctypes.POINTER(bs.DecodeOpts), ctypes.c_void_p]
+    lib.skipsm_decode_ex.restype = ctypes.c_int
+    lib.skipsm_decode_num_splits.argtypes = [ctypes.c_int] * 4
+    lib.skipsm_decode_workspace_size.argtypes = [ctypes.c_int] * 6
+    lib.skipsm_decode_workspace_size.restype = ctypes.c_size_t
+    return lib
+
+
+def traced_decode(lib, q, k, v, lam):
+    """One decode step with every split CTA's start and end time recorded: returns
+    (times [B][Hkv][splits][2] ns, kept tiles per CTA [B][Hkv][splits], splits)."""
+    B, Hq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    ns = lib.skipsm_decode_num_splits(B, Hkv, Skv, 0)
+    ws = torch.empty(lib.skipsm_decode_workspace_size(B, Hq, Hkv, Skv, D, 0), dtype=torch.uint8,
+                     device=q.device)
+    o = torch.empty_like(q)
+    nblk = -(-Skv // 64)
+    mask = torch.empty((B, Hkv, nblk), dtype=torch.uint8, device=q.device)
+    buf = torch.zeros(B * Hkv * ns * 2, dtype=torch.int64, device=q.device)
+    opts = bs.DecodeOpts(0, 0.0, None, mask.data_ptr(), 0, 0, None, None)
+    lib.skipsm_debug_decode_trace(buf.data_ptr())
+    s = torch.cuda.current_stream().cuda_stream
+    rc = lib.skipsm_decode_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv,
+                              Skv, D, float(lam), None, ws.data_ptr(), ws.numel(), ctypes.byref(opts),
+                              s)
+    assert rc == 0
+    st = ctypes.c_int(0)
+    assert lib.skipsm_check(s, ctypes.byref(st)) == 0 and st.value == 0
+    lib.skipsm_debug_decode_trace(None)
+    per = -(-nblk // ns)
+    m = mask.cpu().numpy()
+    kept = np.zeros((B, Hkv, ns), dtype=np.int64)
+    for sp in range(ns):
+        kept[:, :, sp] = (m[:, :, sp * per:(sp + 1) * per] == 0).sum(axis=2)
+    return buf.view(B, Hkv, ns, 2).cpu().numpy(), kept, ns
+
+
+def tail_stats(times, slots):
+    """Makespan, and the share of it during which fewer than half of the CTA slots are busy."""
+    t = times.reshape(-1, 2)
+    t0, t1 = t[:, 0].min(), t[:, 1].max()
+    ev = sorted([(a, 1) for a in t[:, 0]] + [(b, -1) for b in t[:, 1]])
+    active, last, low = 0, t0, 0
+    for when, d in ev:
+        if active < slots // 2:
+            low += when - last
+        active += d
+        last = when
+    dur = t[:, 1] - t[:, 0]
+    return {"makespan_us": (t1 - t0) / 1e3, "share_below_half_busy": low / (t1 - t0),
+            "cta_us_median": float(np.median(dur)) / 1e3, "cta_us_max": float(dur.max()) / 1e3}
+
+
+@pytest.mark.parametrize("rho", [0.0, 0.8])
+def test_decode_trace_covers_every_cta(rho):
+    w = synth.WORKLOADS["decode_128k_gqa8"]
+    q, k, v, _ = device_inputs(w)
+    lam = 0.0 if rho == 0.0 else bs.calibrate_decode(q, k, v, rho)[0]
+    lib = decode_trace_library()
+    times, kept, ns = traced_decode(lib, q, k, v, lam)
+    t = times.reshape(-1, 2)
+    assert np.all(t[:, 0] > 0) and np.all(t[:, 1] >= t[:, 0])
+    stats = tail_stats(times, 2 * 148)
+    dur = (t[:, 1] - t[:, 0]).astype(np.float64)
+    corr = float(np.corrcoef(dur, kept.reshape(-1))[0, 1]) if rho > 0 else 0.0
+    print(f"decode 128K rho={rho} lambda={lam:.3e} splits={ns}: {stats}, "
+          f"corr(CTA time, kept V tiles)={corr:.2f}")
