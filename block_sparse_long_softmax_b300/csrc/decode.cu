@@ -89,7 +89,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t never_bar = bar0 + 8u * (2 * NK + 2 * NV + kNDec);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
 
-  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
+  // Launch order: split-major, the last split of every (batch, kv head) first.  The last
+  // split holds the most recent keys, where the most tiles are kept, so the heaviest CTAs
+  // start in the first wave and the lightest (first splits) fill the tail.
+  const int lin = blockIdx.x + p.nsplit * (blockIdx.y + p.Hkv * blockIdx.z);
+  const int ngroups = p.Hkv * static_cast<int>(gridDim.z);
+  const int grp_id = lin % ngroups;
+  const int split = p.nsplit - 1 - lin / ngroups, hkv = grp_id % p.Hkv, b = grp_id / p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #if SKIPSM_TRACE
   const size_t cta_lin = (static_cast<size_t>(b) * p.Hkv + hkv) * p.nsplit + split;
