@@ -238,10 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&qmap);
         const int zq = b * p.Hq + hq;
         mbar_arrive_expect_tx(qfull, 2 * C::kQTileBytes);
+        // Q is read once: first out of L2, so that the kv head's K and V stay
+        const uint64_t pol = l2_policy_evict_first();
         for (int x = 0; x < 2; ++x)
           for (int h = 0; h < C::kAtoms; ++h)
-            tma_load_3d(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull,
-                        h * C::kAtomElems, qrow0 + x * kQRows, zq);
+            tma_load_3d_hint(sQ + x * C::kQTileBytes + h * kQRows * 128, &qmap, qfull,
+                             h * C::kAtomElems, qrow0 + x * kQRows, zq, pol);
       }
       // with VE the V ring holds only the kept tiles, in order: the n-th loaded V tile
       // uses stage n % NV
@@ -758,13 +760,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               lse2 = -INFINITY;
             }
           }
+          const uint64_t opol = l2_policy_evict_first();   // O is written once
 #pragma unroll
           for (int i = 0; i < D / 8; ++i)
-            dst[i] = make_uint4(
+            st_global_v4_hint(dst + i, make_uint4(
                 pack_bf16x2(__uint_as_float(ov[8 * i]) * inv, __uint_as_float(ov[8 * i + 1]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv));
+                pack_bf16x2(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv)), opol);
           if (p.lse)
             p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Sq + t.row] = lse2 * 0.69314718055994531f;
         }
