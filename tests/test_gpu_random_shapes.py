@@ -22,8 +22,8 @@ from gpu_helpers import ATOL, RTOL, assert_masks, device_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
-N_PREFILL = 60
-N_DECODE = 40
+N_PREFILL = 150
+N_DECODE = 100
 
 
 def _prefill_case(i):
