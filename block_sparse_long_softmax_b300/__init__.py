@@ -40,7 +40,8 @@ class PrefillOpts(ctypes.Structure):
                 ("qk_format", ctypes.c_int), ("qk_descale", ctypes.c_float),
                 ("block_mask", ctypes.c_void_p), ("inject_wait_timeout", ctypes.c_int),
                 ("status", ctypes.c_void_p), ("v_format", ctypes.c_int),
-                ("v_descale", ctypes.c_float), ("v_load", ctypes.c_int)]
+                ("v_descale", ctypes.c_float), ("v_load", ctypes.c_int),
+                ("sync_check", ctypes.c_int)]
 
 
 EXP_MODES = {"exact": 0, "pot": 1}
@@ -65,7 +66,8 @@ class DecodeOpts(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("lse", ctypes.c_void_p), ("skip_mask", ctypes.c_void_p),
                 ("wait_limit_ms", ctypes.c_int), ("inject_wait_timeout", ctypes.c_int),
-                ("block_mask", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+                ("block_mask", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("sync_check", ctypes.c_int)]
 
 
 class Calibration(ctypes.Structure):
@@ -174,7 +176,8 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
             wait_limit_ms: int = 0, exp_mode: str = "exact",
             qk_descale: float = 0.0, block_mask=None,
             inject_wait_timeout: bool = False, status=None,
-            v_descale: float = 0.0, v_load: str = "default") -> PrefillOut:
+            v_descale: float = 0.0, v_load: str = "default",
+            sync_check: bool = False) -> PrefillOut:
     """Skip Softmax prefill: q [B][Hq][Sq][D], k/v [B][Hkv][Skv][D] CUDA tensors.
 
     q and k are bf16, or both float8_e4m3fn (the FP8/BF16 mixed-precision path, D = 128:
@@ -186,6 +189,7 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
     tensor [B][Hq][ceil(Sq/tile_q)][ceil(Skv/tile_k)] of the pairs to visit.
     status: optional int32 CUDA tensor of one element that receives this call's
     device status (a timed-out wait's site) instead of the library's shared word.
+    sync_check: wait for the stream and raise if one of this call's kernel waits timed out.
     """
     import torch
     lib = library()
@@ -215,7 +219,7 @@ def prefill(q, k, v, lam: float, causal: bool = True, *, tile_q: int = 0, tile_k
                        ptr(vis).value, int(wait_limit_ms), _exp_mode(exp_mode), 1 if fp8 else 0,
                        float(qk_descale), ptr(block_mask).value,
                        1 if inject_wait_timeout else 0, _status_ptr(status), 1 if v8 else 0,
-                       float(v_descale), _v_load(v_load))
+                       float(v_descale), _v_load(v_load), 1 if sync_check else 0)
     _raise(lib.skipsm_prefill_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Sq, Skv, D,
                                  1 if causal else 0, float(lam), ptr(cnt), ctypes.byref(opts),
                                  _P(_stream(stream))))
@@ -242,11 +246,12 @@ class DecodeOut:
 def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0.0,
            return_lse: bool = False, return_mask: bool = False, workspace=None, out=None,
            skip_counts=None, stream=None, wait_limit_ms: int = 0,
-           inject_wait_timeout: bool = False, block_mask=None, status=None) -> DecodeOut:
+           inject_wait_timeout: bool = False, block_mask=None, status=None,
+           sync_check: bool = False) -> DecodeOut:
     """Skip Softmax decode: q [B][Hq][D], k/v [B][Hkv][Skv][D] bf16 CUDA tensors.
 
     block_mask: optional uint8/bool CUDA tensor [B][Hkv][ceil(Skv/64)] of the key tiles
-    to visit (nonzero = visit).  status: as for prefill.
+    to visit (nonzero = visit).  status, sync_check: as for prefill.
     """
     import torch
     lib = library()
@@ -270,7 +275,7 @@ def decode(q, k, v, lam: float, *, num_splits: int = 0, softmax_scale: float = 0
                             f"of shape {(B, Hkv, nblk)}")
     opts = DecodeOpts(int(num_splits), float(softmax_scale), ptr(lse).value, ptr(mask).value,
                       int(wait_limit_ms), 1 if inject_wait_timeout else 0, ptr(block_mask).value,
-                      _status_ptr(status))
+                      _status_ptr(status), 1 if sync_check else 0)
     _raise(lib.skipsm_decode_ex(ptr(q), ptr(k), ptr(v), ptr(o), B, Hq, Hkv, Skv, D, float(lam),
                                 ptr(cnt), ptr(ws), ws.numel() * ws.element_size(),
                                 ctypes.byref(opts), _P(_stream(stream))))

@@ -218,6 +218,20 @@ skipsm_status skipsm_check(void* stream, int* device_status) {
   return SKIPSM_OK;
 }
 
+// The sync_check option: wait for the stream, then report the call's device status (its own
+// word, left as it is, or the shared word, read and cleared as by skipsm_check).
+static skipsm_status sync_and_check(cudaStream_t s, int* own) {
+  if (!own) return skipsm_check(s, nullptr);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, own, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (v) return fail(SKIPSM_ERR_TIMEOUT, "a kernel wait exceeded its bound (site %d)", v);
+  t_last_error[0] = '\0';
+  return SKIPSM_OK;
+}
+
 // ------------------------------------------------------------------ prefill
 skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, void* o, int B,
                                 int Hq, int Hkv, int Sq, int Skv, int D, int causal, float lambda,
@@ -319,6 +333,7 @@ skipsm_status skipsm_prefill_ex(const void* q, const void* k, const void* v, voi
       (e = cudaMemsetAsync(op.skip_mask, 2, static_cast<size_t>(B) * Hq * p.nqt * p.nkt, s)))
     return cuda_fail(e, "init skip_mask");
   if ((e = launch_prefill(qmap, kmap, vmap, p, s))) return cuda_fail(e, "prefill launch");
+  if (op.sync_check) return sync_and_check(s, op.status);
   return SKIPSM_OK;
 }
 
@@ -458,6 +473,7 @@ skipsm_status skipsm_decode_ex(const void* q, const void* k, const void* v, void
   c.lse = op.lse;
   c.Hq = Hq; c.D = D; c.nsplit = ns;
   if ((e = launch_combine(c, B, s))) return cuda_fail(e, "decode combine launch");
+  if (op.sync_check) return sync_and_check(s, op.status);
   return SKIPSM_OK;
 }
 

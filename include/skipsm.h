@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define SKIPSM_VERSION 107
+#define SKIPSM_VERSION 108
 
 typedef enum skipsm_status {
   SKIPSM_OK = 0,
@@ -144,6 +144,11 @@ typedef struct skipsm_prefill_opts {
                              tile, ahead of the vote; 2 = only once a query tile of the CTA keeps
                              the key tile (bf16 v, D = 128, tile_k = 128, exp_mode = 0; other
                              configurations fall back to 1).  Results are identical. */
+  int sync_check;         /* nonzero: the call waits for `stream` before it returns and reports
+                             its kernels' device status — SKIPSM_ERR_TIMEOUT if a wait timed out
+                             (the site is in skipsm_last_error()).  With `status` given it reads
+                             that word and leaves it as it is; otherwise it reads and clears the
+                             shared word, as skipsm_check() does.  0 = return once enqueued. */
 } skipsm_prefill_opts;
 
 /*
@@ -214,6 +219,8 @@ typedef struct skipsm_decode_opts {
                               list is kept in shared memory (2 bytes per tile of the split);
                               SKIPSM_ERR_UNSUPPORTED if it does not fit. */
   int* status;            /* optional per-call device status word, as in skipsm_prefill_opts */
+  int sync_check;         /* nonzero: wait for `stream` and report the device status before
+                             returning, as in skipsm_prefill_opts */
 } skipsm_decode_opts;
 
 /*

@@ -54,7 +54,7 @@ def test_noalloc_scratch_fits_both_decode_workloads(lib):
 
 
 def test_version(lib):
-    assert lib.skipsm_version() == 107
+    assert lib.skipsm_version() == 108
 
 
 P = 0x10000  # a 16-byte aligned fake device address; validation never dereferences it

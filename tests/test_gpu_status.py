@@ -56,3 +56,38 @@ def test_status_must_be_an_int32_device_word():
     q, k, v, _ = device_inputs(w)
     with pytest.raises(TypeError):
         bs.decode(q, k, v, 1e-3, status=torch.zeros(1, dtype=torch.int64, device=q.device))
+
+
+@pytest.mark.parametrize("own_word", [False, True])
+def test_sync_check_reports_the_timeout(own_word):
+    """sync_check: the call waits for the stream and returns SKIPSM_ERR_TIMEOUT (4) when one of
+    its waits ran out; the shared word is read and cleared, a caller's own word is left set."""
+    w = synth.WORKLOADS["prefill_32k_gqa8"].with_(B=1, Hq=2, Hkv=1, Sq=300, Skv=300, window=64)
+    q, k, v, _ = device_inputs(w)
+    st = torch.zeros(1, dtype=torch.int32, device=q.device) if own_word else None
+    with pytest.raises(bs.SkipsmError) as e:
+        bs.prefill(q, k, v, 1e-3, wait_limit_ms=20, inject_wait_timeout=True, status=st,
+                   sync_check=True)
+    assert e.value.status == 4 and "site 25" in str(e.value)
+    assert bs.check() == 0            # cleared by the call, or never set
+    if own_word:
+        assert int(st.item()) == 25
+    # a clean call with sync_check returns normally and is correct
+    out = bs.prefill(q, k, v, 1e-3, sync_check=True)
+    ref = bs.prefill(q, k, v, 1e-3)
+    torch.cuda.synchronize()
+    assert torch.equal(out.o, ref.o)
+
+
+def test_decode_sync_check():
+    w = synth.WORKLOADS["decode_32k_gqa8"].with_(B=1, Hq=8, Hkv=1, Skv=1024, window=128)
+    q, k, v, _ = device_inputs(w)
+    with pytest.raises(bs.SkipsmError) as e:
+        bs.decode(q, k, v, 1e-3, num_splits=1, wait_limit_ms=20, inject_wait_timeout=True,
+                  sync_check=True)
+    assert e.value.status == 4 and "site 7" in str(e.value)
+    assert bs.check() == 0
+    out = bs.decode(q, k, v, 1e-3, sync_check=True)
+    ref = bs.decode(q, k, v, 1e-3)
+    torch.cuda.synchronize()
+    assert torch.equal(out.o, ref.o)
